@@ -1,0 +1,734 @@
+// C ABI of the BLOOM decode engine: validation, workspace, launch sequences,
+// CUDA-graph replay of the decode step.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/bloom.h"
+#include "kernels.h"
+
+using namespace bloom;
+
+// ----------------------------------------------------------------- errors
+static thread_local std::string g_err;
+
+static bloom_status fail(bloom_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+#define CK(call)                                                                         \
+    do {                                                                                 \
+        cudaError_t e_ = (call);                                                         \
+        if (e_ != cudaSuccess)                                                           \
+            return fail(BLOOM_E_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                             \
+    } while (0)
+
+extern "C" const char *bloom_last_error(void) { return g_err.c_str(); }
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// ----------------------------------------------------------------- KV layout
+struct KvLayout {
+    size_t next_pos, pos, k, v, total, layer;   // layer = bytes of one layer's K (or V)
+};
+
+static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq) {
+    KvLayout L;
+    const size_t d = (size_t)(c.hidden / c.n_head);
+    size_t off = 256;
+    L.next_pos = off;
+    off = align256(off + 4 * (size_t)batch);
+    L.pos = off;
+    off = align256(off + 4 * (size_t)batch * max_seq);
+    L.layer = (size_t)batch * c.n_head * max_seq * d * 2;
+    L.k = off;
+    off = align256(off + L.layer * c.n_layer);
+    L.v = off;
+    off = align256(off + L.layer * c.n_layer);
+    L.total = off;
+    return L;
+}
+
+// ----------------------------------------------------------------- model
+struct GraphEntry {
+    void *kvbuf;
+    const void *next;
+    void *out;
+    void *logits;
+    int B;
+    cudaGraphExec_t exec;
+};
+
+struct bloom_model {
+    bloom_config cfg;
+    const void *word_emb, *emb_ln_g, *emb_ln_b, *lnf_g, *lnf_b;
+    std::vector<bloom_layer_weights> layers;
+    int dev = 0, num_sms = 0;
+    int d = 0;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    uint16_t *x = nullptr, *a = nullptr, *q = nullptr, *o = nullptr, *u = nullptr,
+             *xl = nullptr;
+    float *slopes = nullptr;
+    unsigned long long *best = nullptr;
+    int *head_ticket = nullptr;
+    float *attn_part = nullptr;
+    int *attn_ticket = nullptr;
+    int *err = nullptr;
+    int *last = nullptr;
+    int32_t *tok = nullptr;       // [max_batch] device feedback token
+    int32_t *gen = nullptr;       // [max_seq][max_batch]
+    int32_t *ptok = nullptr;      // [max_tokens] prompt ids (bloom_generate)
+    uint8_t *pmask = nullptr;     // [max_tokens]
+    cudaStream_t cap = nullptr;
+    std::vector<GraphEntry> graphs;
+};
+
+static int attn_splits(const bloom_model *m, int B, int max_seq) {
+    const int want = (2 * m->num_sms + B * m->cfg.n_head - 1) / (B * m->cfg.n_head);
+    int cap = (max_seq + 31) / 32;
+    int s = want < cap ? want : cap;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return s < 1 ? 1 : s;
+}
+
+static bloom_status check_linear(const bloom_linear &l, int int8, int N, int K, const char *nm,
+                                 int layer) {
+    (void)N;
+    if (!l.w) return fail(BLOOM_E_INVALID, "layer %d %s: null weight", layer, nm);
+    if (!aligned16(l.w)) return fail(BLOOM_E_INVALID, "layer %d %s: weight not 16-byte aligned", layer, nm);
+    if (int8 && !l.scale) return fail(BLOOM_E_INVALID, "layer %d %s: int8 weight without scales", layer, nm);
+    if (!int8 && l.scale) return fail(BLOOM_E_INVALID, "layer %d %s: scales given for bf16 weight", layer, nm);
+    if (K % (int8 ? 16 : 8)) return fail(BLOOM_E_UNSUPPORTED, "layer %d %s: K=%d not a multiple of %d", layer, nm, K, int8 ? 16 : 8);
+    return BLOOM_OK;
+}
+
+static bloom_status validate_config(const bloom_config *c) {
+    if (!c) return fail(BLOOM_E_INVALID, "null config");
+    if (c->n_layer < 1 || c->hidden < 8 || c->n_head < 1 || c->ffn < 16 || c->vocab < 1)
+        return fail(BLOOM_E_INVALID, "non-positive size in config");
+    if (c->hidden % c->n_head) return fail(BLOOM_E_INVALID, "hidden %% n_head != 0");
+    const int d = c->hidden / c->n_head;
+    if (d != 64 && d != 128) return fail(BLOOM_E_UNSUPPORTED, "head_dim %d (64 or 128 supported)", d);
+    if (c->hidden % 16 || c->hidden > kMaxHidden)
+        return fail(BLOOM_E_UNSUPPORTED, "hidden %d (multiple of 16, <= %d)", c->hidden, kMaxHidden);
+    if (c->ffn % 16) return fail(BLOOM_E_UNSUPPORTED, "ffn %d not a multiple of 16", c->ffn);
+    if (!(c->ln_eps > 0.f)) return fail(BLOOM_E_INVALID, "ln_eps must be > 0");
+    if (c->weight_dtype != BLOOM_WEIGHT_BF16 && c->weight_dtype != BLOOM_WEIGHT_INT8)
+        return fail(BLOOM_E_INVALID, "weight_dtype %d", c->weight_dtype);
+    if (c->max_batch < 1 || c->max_batch > kMaxBatch)
+        return fail(BLOOM_E_UNSUPPORTED, "max_batch %d (1..%d)", c->max_batch, kMaxBatch);
+    if (c->max_tokens < c->max_batch) return fail(BLOOM_E_INVALID, "max_tokens < max_batch");
+    if (c->max_seq < 1) return fail(BLOOM_E_INVALID, "max_seq < 1");
+    return BLOOM_OK;
+}
+
+extern "C" size_t bloom_kv_bytes(const bloom_config *cfg, int32_t batch, int32_t max_seq) {
+    if (validate_config(cfg) != BLOOM_OK || batch < 1 || max_seq < 1) return 0;
+    return kv_layout(*cfg, batch, max_seq).total;
+}
+
+extern "C" bloom_status bloom_destroy(bloom_model *m) {
+    if (!m) return BLOOM_OK;
+    cudaSetDevice(m->dev);
+    for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
+    if (m->cap) cudaStreamDestroy(m->cap);
+    if (m->ws) cudaFree(m->ws);
+    delete m;
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weights *w,
+                                     bloom_model **out) {
+    if (!out) return fail(BLOOM_E_INVALID, "null output handle");
+    *out = nullptr;
+    bloom_status st = validate_config(cfg);
+    if (st) return st;
+    if (!w || !w->word_emb || !w->emb_ln_g || !w->emb_ln_b || !w->lnf_g || !w->lnf_b || !w->layers)
+        return fail(BLOOM_E_INVALID, "null top-level weight pointer");
+    if (!aligned16(w->word_emb) || !aligned16(w->emb_ln_g) || !aligned16(w->emb_ln_b) ||
+        !aligned16(w->lnf_g) || !aligned16(w->lnf_b))
+        return fail(BLOOM_E_INVALID, "top-level weights must be 16-byte aligned");
+    const int h = cfg->hidden, F = cfg->ffn, i8 = cfg->weight_dtype == BLOOM_WEIGHT_INT8;
+    for (int l = 0; l < cfg->n_layer; ++l) {
+        const bloom_layer_weights &L = w->layers[l];
+        if (!L.ln1_g || !L.ln1_b || !L.ln2_g || !L.ln2_b)
+            return fail(BLOOM_E_INVALID, "layer %d: null LayerNorm pointer", l);
+        if (!aligned16(L.ln1_g) || !aligned16(L.ln1_b) || !aligned16(L.ln2_g) || !aligned16(L.ln2_b))
+            return fail(BLOOM_E_INVALID, "layer %d: LayerNorm params not 16-byte aligned", l);
+        if ((st = check_linear(L.qkv, i8, 3 * h, h, "qkv", l))) return st;
+        if ((st = check_linear(L.o, i8, h, h, "o", l))) return st;
+        if ((st = check_linear(L.up, i8, F, h, "up", l))) return st;
+        if ((st = check_linear(L.down, i8, h, F, "down", l))) return st;
+    }
+    bloom_model *m = new bloom_model();
+    m->cfg = *cfg;
+    m->word_emb = w->word_emb;
+    m->emb_ln_g = w->emb_ln_g;
+    m->emb_ln_b = w->emb_ln_b;
+    m->lnf_g = w->lnf_g;
+    m->lnf_b = w->lnf_b;
+    m->layers.assign(w->layers, w->layers + cfg->n_layer);
+    m->d = h / cfg->n_head;
+    cudaError_t e = cudaGetDevice(&m->dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->dev);
+    if (e != cudaSuccess) {
+        delete m;
+        return fail(BLOOM_E_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    // workspace carve-up
+    const size_t MT = (size_t)cfg->max_tokens, MB = (size_t)cfg->max_batch;
+    const size_t n = (size_t)cfg->n_head, d = (size_t)m->d;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    const size_t o_x = take(MT * h * 2), o_a = take(MT * h * 2), o_q = take(MT * h * 2),
+                 o_o = take(MT * h * 2), o_u = take(MT * F * 2), o_xl = take(MB * h * 2),
+                 o_sl = take(n * 4), o_best = take(MB * 8), o_ht = take(4),
+                 o_ap = take(MB * n * kMaxSplits * (d + 2) * 4), o_at = take(MB * n * 4),
+                 o_err = take(4), o_last = take(MB * 4), o_tok = take(MB * 4),
+                 o_gen = take((size_t)cfg->max_seq * MB * 4), o_ptok = take(MT * 4),
+                 o_pmask = take(MT);
+    m->ws_bytes = off;
+    e = cudaMalloc(&m->ws, m->ws_bytes);
+    if (e != cudaSuccess) {
+        delete m;
+        cudaGetLastError();
+        return fail(BLOOM_E_OOM, "workspace of %zu bytes: %s", off, cudaGetErrorString(e));
+    }
+    char *base = (char *)m->ws;
+    m->x = (uint16_t *)(base + o_x);
+    m->a = (uint16_t *)(base + o_a);
+    m->q = (uint16_t *)(base + o_q);
+    m->o = (uint16_t *)(base + o_o);
+    m->u = (uint16_t *)(base + o_u);
+    m->xl = (uint16_t *)(base + o_xl);
+    m->slopes = (float *)(base + o_sl);
+    m->best = (unsigned long long *)(base + o_best);
+    m->head_ticket = (int *)(base + o_ht);
+    m->attn_part = (float *)(base + o_ap);
+    m->attn_ticket = (int *)(base + o_at);
+    m->err = (int *)(base + o_err);
+    m->last = (int *)(base + o_last);
+    m->tok = (int32_t *)(base + o_tok);
+    m->gen = (int32_t *)(base + o_gen);
+    m->ptok = (int32_t *)(base + o_ptok);
+    m->pmask = (uint8_t *)(base + o_pmask);
+    // ALiBi slopes, once: largest power of two p <= n heads gets 2^(-8i/p),
+    // i = 1..p; the remaining heads take 2^(-8i/(2p)) for odd i = 1, 3, ...
+    std::vector<float> sl(n);
+    int p2 = 1;
+    while (p2 * 2 <= (int)n) p2 *= 2;
+    for (int i = 1; i <= p2; ++i) sl[i - 1] = (float)pow(2.0, -8.0 * i / p2);
+    for (int j = 0; j < (int)n - p2; ++j) sl[p2 + j] = (float)pow(2.0, -8.0 * (2 * j + 1) / (2.0 * p2));
+    bloom_status st2 = BLOOM_OK;
+    if (cudaMemset(m->ws, 0, m->ws_bytes) != cudaSuccess ||
+        cudaMemcpy(m->slopes, sl.data(), n * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking) != cudaSuccess ||
+        linear_prepare() != cudaSuccess) {
+        st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    if (st2) {
+        bloom_destroy(m);
+        return st2;
+    }
+    *out = m;
+    return BLOOM_OK;
+}
+
+static bloom_status check_kv(const bloom_model *m, const bloom_kv *kv) {
+    if (!m) return fail(BLOOM_E_INVALID, "null model");
+    if (!kv || !kv->buf) return fail(BLOOM_E_INVALID, "null kv");
+    if (kv->batch < 1 || kv->batch > m->cfg.max_batch)
+        return fail(BLOOM_E_CAPACITY, "kv batch %d above max_batch %d", kv->batch, m->cfg.max_batch);
+    if (kv->max_seq < 1) return fail(BLOOM_E_INVALID, "kv max_seq %d", kv->max_seq);
+    if (kv->bytes < kv_layout(m->cfg, kv->batch, kv->max_seq).total)
+        return fail(BLOOM_E_INVALID, "kv buffer too small");
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
+                                      int32_t batch, int32_t max_seq, void *stream) {
+    if (!m || !kv || !buf) return fail(BLOOM_E_INVALID, "null argument");
+    if (((uintptr_t)buf & 255u) != 0) return fail(BLOOM_E_INVALID, "kv buffer not 256-byte aligned");
+    if (batch < 1 || batch > m->cfg.max_batch)
+        return fail(BLOOM_E_CAPACITY, "batch %d outside 1..max_batch %d", batch, m->cfg.max_batch);
+    if (max_seq < 1 || max_seq > m->cfg.max_seq)
+        return fail(BLOOM_E_CAPACITY, "max_seq %d outside 1..%d", max_seq, m->cfg.max_seq);
+    const KvLayout L = kv_layout(m->cfg, batch, max_seq);
+    if (bytes < L.total) return fail(BLOOM_E_INVALID, "kv buffer %zu < %zu bytes", bytes, L.total);
+    cudaStream_t s = (cudaStream_t)stream;
+    CK(cudaMemsetAsync(buf, 0, L.pos, s));
+    CK(cudaMemsetAsync((char *)buf + L.pos, 0xff, L.k - L.pos, s));
+    kv->buf = buf;
+    kv->bytes = bytes;
+    kv->batch = batch;
+    kv->max_seq = max_seq;
+    kv->len = 0;
+    return BLOOM_OK;
+}
+
+// pointers into a kv buffer
+struct KvPtrs {
+    int *len, *next_pos, *pos;
+    uint16_t *k, *v;
+    size_t layer_elems;
+};
+static KvPtrs kv_ptrs(const bloom_model *m, const bloom_kv *kv) {
+    const KvLayout L = kv_layout(m->cfg, kv->batch, kv->max_seq);
+    char *b = (char *)kv->buf;
+    KvPtrs p;
+    p.len = (int *)b;
+    p.next_pos = (int *)(b + L.next_pos);
+    p.pos = (int *)(b + L.pos);
+    p.k = (uint16_t *)(b + L.k);
+    p.v = (uint16_t *)(b + L.v);
+    p.layer_elems = L.layer / 2;
+    return p;
+}
+
+static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, int M, int N,
+                           int K, int epi) {
+    LinearArgs a;
+    a.w = l.w;
+    a.scale = (const uint16_t *)l.scale;
+    a.bias = (const uint16_t *)l.bias;
+    a.x = x;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.int8 = int8;
+    a.epi = epi;
+    return a;
+}
+
+// One decoder layer over M tokens.  Decode: M = B sequences, slot *len.
+// Prefill: M = B*T tokens, slots [0, T).
+static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int max_seq, int l,
+                                 int M, int T, int splits, uint16_t *x, cudaStream_t s) {
+    const bloom_config &c = m->cfg;
+    const bloom_layer_weights &L = m->layers[l];
+    const int h = c.hidden, F = c.ffn, n = c.n_head, d = m->d;
+    const int i8 = c.weight_dtype == BLOOM_WEIGHT_INT8;
+    const float eps = c.ln_eps;
+    cudaError_t e;
+    if ((e = launch_layernorm(x, (const uint16_t *)L.ln1_g, (const uint16_t *)L.ln1_b, M, h, eps,
+                              m->a, 1, nullptr, s)))
+        return e;
+    LinearArgs q = lin_args(L.qkv, i8, m->a, M, 3 * h, h, EPI_QKV);
+    q.q_out = m->q;
+    q.k_cache = kp.k + kp.layer_elems * l;
+    q.v_cache = kp.v + kp.layer_elems * l;
+    q.len_ptr = kp.len;
+    q.T = T;
+    q.n_head = n;
+    q.head_dim = d;
+    q.max_seq = max_seq;
+    q.err = m->err;
+    if ((e = launch_linear(q, m->num_sms, s))) return e;
+    if (T == 0) {
+        AttnDecodeArgs at;
+        at.q = m->q;
+        at.k = q.k_cache;
+        at.v = q.v_cache;
+        at.pos = kp.pos;
+        at.slopes = m->slopes;
+        at.len_ptr = kp.len;
+        at.B = B;
+        at.n = n;
+        at.d = d;
+        at.max_seq = max_seq;
+        at.splits = splits;
+        at.scale = (float)(1.0 / sqrt((double)d));
+        at.part = m->attn_part;
+        at.ticket = m->attn_ticket;
+        at.o = m->o;
+        if ((e = launch_attn_decode(at, s))) return e;
+    } else {
+        AttnPrefillArgs at;
+        at.q = m->q;
+        at.k = q.k_cache;
+        at.v = q.v_cache;
+        at.pos = kp.pos;
+        at.slopes = m->slopes;
+        at.B = B;
+        at.T = T;
+        at.n = n;
+        at.d = d;
+        at.max_seq = max_seq;
+        at.scale = (float)(1.0 / sqrt((double)d));
+        at.o = m->o;
+        if ((e = launch_attn_prefill(at, s))) return e;
+    }
+    LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID);
+    od.out = x;
+    if ((e = launch_linear(od, m->num_sms, s))) return e;
+    if ((e = launch_layernorm(x, (const uint16_t *)L.ln2_g, (const uint16_t *)L.ln2_b, M, h, eps,
+                              m->a, 1, nullptr, s)))
+        return e;
+    LinearArgs up = lin_args(L.up, i8, m->a, M, F, h, EPI_GELU);
+    up.out = m->u;
+    if ((e = launch_linear(up, m->num_sms, s))) return e;
+    LinearArgs dn = lin_args(L.down, i8, m->u, M, h, F, EPI_RESID);
+    dn.out = x;
+    return launch_linear(dn, m->num_sms, s);
+}
+
+// ln_f + tied head + argmax on rows of `x` (row r at x[(r*stride + last[r]) * h]).
+static cudaError_t enqueue_head(bloom_model *m, const uint16_t *x, int B, int stride,
+                                const int *last, int32_t *out_tokens, float *logits,
+                                int *len_inc, int *next_pos, cudaStream_t s) {
+    const bloom_config &c = m->cfg;
+    cudaError_t e = launch_layernorm(x, (const uint16_t *)m->lnf_g, (const uint16_t *)m->lnf_b, B,
+                                     c.hidden, c.ln_eps, m->xl, stride, last, s);
+    if (e) return e;
+    LinearArgs a;
+    a.w = m->word_emb;
+    a.x = m->xl;
+    a.M = B;
+    a.N = c.vocab;
+    a.K = c.hidden;
+    a.epi = EPI_ARGMAX;
+    a.logits = logits;
+    a.best = m->best;
+    a.ticket = m->head_ticket;
+    a.out_tokens = out_tokens;
+    a.len_inc = len_inc;
+    a.next_pos = next_pos;
+    return launch_linear(a, m->num_sms, s);
+}
+
+static cudaError_t enqueue_decode(bloom_model *m, const bloom_kv *kv, const int32_t *next,
+                                  int32_t *out, float *logits, cudaStream_t s) {
+    const bloom_config &c = m->cfg;
+    const KvPtrs kp = kv_ptrs(m, kv);
+    const int B = kv->batch;
+    const int splits = attn_splits(m, B, kv->max_seq);
+    cudaError_t e = launch_embed(next, B, (const uint16_t *)m->word_emb, c.vocab,
+                                 (const uint16_t *)m->emb_ln_g, (const uint16_t *)m->emb_ln_b,
+                                 c.hidden, c.ln_eps, m->x, kp.len, kp.next_pos, kp.pos,
+                                 kv->max_seq, m->err, s);
+    if (e) return e;
+    for (int l = 0; l < c.n_layer; ++l)
+        if ((e = enqueue_layer(m, kp, B, kv->max_seq, l, B, 0, splits, m->x, s))) return e;
+    return enqueue_head(m, m->x, B, 1, nullptr, out, logits, kp.len, kp.next_pos, s);
+}
+
+extern "C" int32_t bloom_decode_launches(const bloom_model *m) {
+    return m ? 1 + 7 * m->cfg.n_layer + 2 : 0;
+}
+
+extern "C" bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
+                                            int32_t B, int32_t T, void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!mask) return fail(BLOOM_E_INVALID, "null mask");
+    if (B != kv->batch) return fail(BLOOM_E_CAPACITY, "B=%d but kv batch is %d", B, kv->batch);
+    if (T < 1 || T > kv->max_seq) return fail(BLOOM_E_CAPACITY, "T=%d outside 1..%d", T, kv->max_seq);
+    const KvPtrs kp = kv_ptrs(m, kv);
+    CK(launch_prompt_setup(mask, B, T, kp.pos, kv->max_seq, kp.next_pos, m->last, kp.len, m->err,
+                           (cudaStream_t)stream));
+    kv->len = T;
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
+                                      const uint8_t *mask, int32_t B, int32_t T,
+                                      int32_t *out_tokens, float *out_logits, void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!tokens || !mask || !out_tokens) return fail(BLOOM_E_INVALID, "null tokens/mask/out_tokens");
+    if (B != kv->batch) return fail(BLOOM_E_CAPACITY, "B=%d but kv batch is %d", B, kv->batch);
+    if (T < 1 || T > kv->max_seq) return fail(BLOOM_E_CAPACITY, "T=%d outside 1..%d", T, kv->max_seq);
+    if ((long long)B * T > m->cfg.max_tokens)
+        return fail(BLOOM_E_CAPACITY, "B*T=%lld above max_tokens %d", (long long)B * T, m->cfg.max_tokens);
+    const bloom_config &c = m->cfg;
+    cudaStream_t s = (cudaStream_t)stream;
+    const KvPtrs kp = kv_ptrs(m, kv);
+    const int M = B * T;
+    CK(launch_prompt_setup(mask, B, T, kp.pos, kv->max_seq, kp.next_pos, m->last, kp.len, m->err, s));
+    CK(launch_embed(tokens, M, (const uint16_t *)m->word_emb, c.vocab, (const uint16_t *)m->emb_ln_g,
+                    (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, m->x, nullptr, nullptr,
+                    nullptr, 0, m->err, s));
+    for (int l = 0; l < c.n_layer; ++l) CK(enqueue_layer(m, kp, B, kv->max_seq, l, M, T, 1, m->x, s));
+    CK(enqueue_head(m, m->x, B, T, m->last, out_tokens, out_logits, nullptr, nullptr, s));
+    kv->len = T;
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
+                                          int32_t *out_tokens, float *out_logits, void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!next_tokens || !out_tokens) return fail(BLOOM_E_INVALID, "null next_tokens/out_tokens");
+    if (kv->len < 1) return fail(BLOOM_E_INVALID, "decode before prefill");
+    if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full (%d slots)", kv->max_seq);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (m->cfg.flags & BLOOM_FLAG_NO_GRAPH) {
+        CK(enqueue_decode(m, kv, next_tokens, out_tokens, out_logits, s));
+    } else {
+        cudaGraphExec_t exec = nullptr;
+        for (auto &g : m->graphs)
+            if (g.kvbuf == kv->buf && g.next == next_tokens && g.out == out_tokens &&
+                g.logits == out_logits && g.B == kv->batch) {
+                exec = g.exec;
+                break;
+            }
+        if (!exec) {
+            cudaGraph_t graph = nullptr;
+            CK(cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal));
+            cudaError_t e = enqueue_decode(m, kv, next_tokens, out_tokens, out_logits, m->cap);
+            cudaError_t e2 = cudaStreamEndCapture(m->cap, &graph);
+            if (e != cudaSuccess || e2 != cudaSuccess) {
+                if (graph) cudaGraphDestroy(graph);
+                return fail(BLOOM_E_CUDA, "decode capture: %s / %s", cudaGetErrorString(e),
+                            cudaGetErrorString(e2));
+            }
+            e = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (e != cudaSuccess) return fail(BLOOM_E_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+            if (m->graphs.size() >= 16) {
+                cudaGraphExecDestroy(m->graphs.front().exec);
+                m->graphs.erase(m->graphs.begin());
+            }
+            m->graphs.push_back({kv->buf, next_tokens, out_tokens, out_logits, kv->batch, exec});
+        }
+        CK(cudaGraphLaunch(exec, s));
+    }
+    kv->len += 1;
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_check_device(bloom_model *m, void *stream) {
+    if (!m) return fail(BLOOM_E_INVALID, "null model");
+    cudaStream_t s = (cudaStream_t)stream;
+    int flag = 0;
+    CK(cudaMemcpyAsync(&flag, m->err, 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaMemsetAsync(m->err, 0, 4, s));
+    CK(cudaStreamSynchronize(s));
+    if (flag)
+        return fail(BLOOM_E_DEVICE_FLAG, "device flag 0x%x (1: token id out of range, 2: cache "
+                    "slot out of range, 4: prompt row without a token)", flag);
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_generate(bloom_model *m, bloom_kv *kv, const int32_t *tokens_host,
+                                       const uint8_t *mask_host, int32_t B, int32_t T,
+                                       int32_t n_new, int32_t *out_host, void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!tokens_host || !mask_host || !out_host) return fail(BLOOM_E_INVALID, "null host buffer");
+    if (n_new < 1) return fail(BLOOM_E_INVALID, "n_new %d", n_new);
+    if ((long long)T + n_new - 1 > kv->max_seq)
+        return fail(BLOOM_E_CAPACITY, "T + n_new - 1 = %d above kv max_seq %d", T + n_new - 1, kv->max_seq);
+    if ((long long)B * T > m->cfg.max_tokens)
+        return fail(BLOOM_E_CAPACITY, "B*T above max_tokens");
+    if (n_new > m->cfg.max_seq) return fail(BLOOM_E_CAPACITY, "n_new above max_seq");
+    cudaStream_t s = (cudaStream_t)stream;
+    CK(cudaMemcpyAsync(m->ptok, tokens_host, (size_t)B * T * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(m->pmask, mask_host, (size_t)B * T, cudaMemcpyHostToDevice, s));
+    if ((st = bloom_prefill(m, kv, m->ptok, m->pmask, B, T, m->tok, nullptr, stream))) return st;
+    CK(cudaMemcpyAsync(m->gen, m->tok, (size_t)B * 4, cudaMemcpyDeviceToDevice, s));
+    for (int i = 1; i < n_new; ++i) {
+        if ((st = bloom_decode_step(m, kv, m->tok, m->tok, nullptr, stream))) return st;
+        CK(cudaMemcpyAsync(m->gen + (size_t)i * B, m->tok, (size_t)B * 4, cudaMemcpyDeviceToDevice, s));
+    }
+    CK(cudaMemcpyAsync(out_host, m->gen, (size_t)n_new * B * 4, cudaMemcpyDeviceToHost, s));
+    return bloom_check_device(m, stream);
+}
+
+// ----------------------------------------------------------------- layer-level
+extern "C" bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
+                                           void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!x) return fail(BLOOM_E_INVALID, "null x");
+    if (layer < 0 || layer >= m->cfg.n_layer) return fail(BLOOM_E_INVALID, "layer %d", layer);
+    if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full");
+    cudaStream_t s = (cudaStream_t)stream;
+    const KvPtrs kp = kv_ptrs(m, kv);
+    CK(launch_slot_pos(kv->batch, kp.len, kp.next_pos, kp.pos, kv->max_seq, m->err, s));
+    CK(enqueue_layer(m, kp, kv->batch, kv->max_seq, layer, kv->batch, 0,
+                     attn_splits(m, kv->batch, kv->max_seq), (uint16_t *)x, s));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_layer_prefill(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
+                                            int32_t B, int32_t T, void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!x) return fail(BLOOM_E_INVALID, "null x");
+    if (layer < 0 || layer >= m->cfg.n_layer) return fail(BLOOM_E_INVALID, "layer %d", layer);
+    if (B != kv->batch || T < 1 || T > kv->max_seq || (long long)B * T > m->cfg.max_tokens)
+        return fail(BLOOM_E_CAPACITY, "B=%d T=%d", B, T);
+    const KvPtrs kp = kv_ptrs(m, kv);
+    CK(enqueue_layer(m, kp, B, kv->max_seq, layer, B * T, T, 1, (uint16_t *)x, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int32_t *out_tokens,
+                                   float *out_logits, void *stream) {
+    if (!m || !x || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
+    if (B < 1 || B > m->cfg.max_batch) return fail(BLOOM_E_CAPACITY, "B=%d", B);
+    CK(enqueue_head(m, (const uint16_t *)x, B, 1, nullptr, out_tokens, out_logits, nullptr, nullptr,
+                    (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B,
+                                      int32_t *out_tokens, float *out_logits, void *stream) {
+    if (!m || !xn || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
+    if (B < 1 || B > m->cfg.max_batch) return fail(BLOOM_E_CAPACITY, "B=%d", B);
+    if (!aligned16(xn)) return fail(BLOOM_E_INVALID, "xn not 16-byte aligned");
+    LinearArgs a;
+    a.w = m->word_emb;
+    a.x = (const uint16_t *)xn;
+    a.M = B;
+    a.N = m->cfg.vocab;
+    a.K = m->cfg.hidden;
+    a.epi = EPI_ARGMAX;
+    a.logits = out_logits;
+    a.best = m->best;
+    a.ticket = m->head_ticket;
+    a.out_tokens = out_tokens;
+    CK(launch_linear(a, m->num_sms, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32_t n, void *x,
+                                    void *stream) {
+    if (!m || !tokens || !x) return fail(BLOOM_E_INVALID, "null argument");
+    if (n < 1) return fail(BLOOM_E_INVALID, "n=%d", n);
+    const bloom_config &c = m->cfg;
+    CK(launch_embed(tokens, n, (const uint16_t *)m->word_emb, c.vocab, (const uint16_t *)m->emb_ln_g,
+                    (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, (uint16_t *)x, nullptr,
+                    nullptr, nullptr, 0, m->err, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+// ----------------------------------------------------------------- operators
+static int device_sms() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    return sms;
+}
+
+extern "C" bloom_status bloom_op_layernorm(const void *x, const void *g, const void *b,
+                                           int32_t rows, int32_t h, float eps, void *y,
+                                           void *stream) {
+    if (!x || !y) return fail(BLOOM_E_INVALID, "null x/y");
+    if (rows < 0 || h < 8 || h % 8 || h > kMaxHidden) return fail(BLOOM_E_UNSUPPORTED, "h=%d", h);
+    if (!aligned16(x) || !aligned16(y) || (g && !aligned16(g)) || (b && !aligned16(b)))
+        return fail(BLOOM_E_INVALID, "pointers must be 16-byte aligned");
+    CK(launch_layernorm((const uint16_t *)x, (const uint16_t *)g, (const uint16_t *)b, rows, h, eps,
+                        (uint16_t *)y, 1, nullptr, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *x,
+                                        int32_t M, int32_t N, int32_t K, int32_t epilogue, void *y,
+                                        void *stream) {
+    if (!lin || !x || !y) return fail(BLOOM_E_INVALID, "null argument");
+    bloom_status st = check_linear(*lin, int8, N, K, "op", -1);
+    if (st) return st;
+    if (M < 0 || N < 1) return fail(BLOOM_E_INVALID, "M=%d N=%d", M, N);
+    if (epilogue < BLOOM_EPI_STORE || epilogue > BLOOM_EPI_RESID)
+        return fail(BLOOM_E_INVALID, "epilogue %d", epilogue);
+    if (!aligned16(x)) return fail(BLOOM_E_INVALID, "x not 16-byte aligned");
+    LinearArgs a = lin_args(*lin, int8, (const uint16_t *)x, M, N, K, epilogue);
+    a.out = (uint16_t *)y;
+    CK(launch_linear(a, device_sms(), (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
+                                             const void *v_cache, const int32_t *pos,
+                                             const float *slopes, int32_t B, int32_t n_head,
+                                             int32_t d, int32_t max_seq, int32_t len,
+                                             int32_t splits, void *o, void *stream) {
+    if (!q || !k_cache || !v_cache || !pos || !slopes || !o) return fail(BLOOM_E_INVALID, "null argument");
+    if (d != 64 && d != 128) return fail(BLOOM_E_UNSUPPORTED, "d=%d", d);
+    if (B < 1 || n_head < 1 || max_seq < 1 || len < 0 || len >= max_seq)
+        return fail(BLOOM_E_INVALID, "B=%d n=%d max_seq=%d len=%d", B, n_head, max_seq, len);
+    if (splits <= 0) {
+        int want = (2 * device_sms() + B * n_head - 1) / (B * n_head);
+        int cap = (len + 1 + 31) / 32;
+        splits = want < cap ? want : cap;
+        if (splits < 1) splits = 1;
+    }
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    cudaStream_t s = (cudaStream_t)stream;
+    AttnDecodeArgs a;
+    a.q = (const uint16_t *)q;
+    a.k = (const uint16_t *)k_cache;
+    a.v = (const uint16_t *)v_cache;
+    a.pos = pos;
+    a.slopes = slopes;
+    a.len_host = len;
+    a.B = B;
+    a.n = n_head;
+    a.d = d;
+    a.max_seq = max_seq;
+    a.splits = splits;
+    a.scale = (float)(1.0 / sqrt((double)d));
+    void *scratch = nullptr;
+    const size_t part_bytes = align256((size_t)B * n_head * splits * (d + 2) * 4);
+    const size_t bytes = part_bytes + (size_t)B * n_head * 4;
+    CK(cudaMallocAsync(&scratch, bytes, s));
+    cudaError_t e = cudaMemsetAsync(scratch, 0, bytes, s);
+    a.part = (float *)scratch;
+    a.ticket = (int *)((char *)scratch + part_bytes);
+    a.o = (uint16_t *)o;
+    if (e == cudaSuccess) e = launch_attn_decode(a, s);
+    cudaError_t e2 = cudaFreeAsync(scratch, s);
+    CK(e);
+    CK(e2);
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, int32_t M,
+                                               int32_t V, int32_t K, int32_t *out_tokens,
+                                               float *out_logits, void *stream) {
+    if (!x || !emb || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
+    if (M < 1 || M > kMaxBatch || V < 1 || K < 8 || K % 8)
+        return fail(BLOOM_E_UNSUPPORTED, "M=%d V=%d K=%d", M, V, K);
+    if (!aligned16(x) || !aligned16(emb)) return fail(BLOOM_E_INVALID, "pointers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    void *scratch = nullptr;
+    const size_t bytes = 256 + (size_t)M * 8;
+    CK(cudaMallocAsync(&scratch, bytes, s));
+    cudaError_t e = cudaMemsetAsync(scratch, 0, bytes, s);
+    LinearArgs a;
+    a.w = emb;
+    a.x = (const uint16_t *)x;
+    a.M = M;
+    a.N = V;
+    a.K = K;
+    a.epi = EPI_ARGMAX;
+    a.logits = out_logits;
+    a.ticket = (int *)scratch;
+    a.best = (unsigned long long *)((char *)scratch + 256);
+    a.out_tokens = out_tokens;
+    if (e == cudaSuccess) e = launch_linear(a, device_sms(), s);
+    cudaError_t e2 = cudaFreeAsync(scratch, s);
+    CK(e);
+    CK(e2);
+    return BLOOM_OK;
+}

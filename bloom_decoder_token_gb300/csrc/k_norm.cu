@@ -1,0 +1,161 @@
+// LayerNorm, embedding gather + LayerNorm, and the small step-state kernels.
+//
+// One CTA normalises one row, all its values held in registers: float32 mean,
+// then float32 biased variance of the deviations (two passes over registers,
+// no E[x^2] - mean^2 cancellation), eps inside the square root, affine gamma /
+// beta, bf16 out.  "DeepSpeed Inference", III.B: all micro-operations of the
+// layer norm, its reductions included, run in one kernel because the reduced
+// dimension stays inside one thread block.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bloom {
+
+constexpr int kLnThreads = 256;
+constexpr int kLnWarps = kLnThreads / kWarp;
+constexpr int kLnChunks = kMaxHidden / 8 / kLnThreads;   // 8-element chunks per thread
+
+__device__ __forceinline__ void ln_row(const uint16_t *__restrict__ src,
+                                       const uint16_t *__restrict__ g,
+                                       const uint16_t *__restrict__ b, int h, float eps,
+                                       uint16_t *__restrict__ dst, float *red) {
+    const int nch = h / 8;
+    float v[kLnChunks][8];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnChunks; ++i) {
+        const int c = threadIdx.x + i * kLnThreads;
+        if (c < nch) {
+            unpack8(*reinterpret_cast<const uint4 *>(src + (size_t)c * 8), v[i]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s += v[i][e];
+        }
+    }
+    const float mean = block_sum<kLnWarps>(s, red) / (float)h;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnChunks; ++i) {
+        const int c = threadIdx.x + i * kLnThreads;
+        if (c < nch) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float dlt = v[i][e] - mean;
+                q += dlt * dlt;
+            }
+        }
+    }
+    const float var = block_sum<kLnWarps>(q, red) / (float)h;
+    const float rstd = rsqrtf(var + eps);
+#pragma unroll
+    for (int i = 0; i < kLnChunks; ++i) {
+        const int c = threadIdx.x + i * kLnThreads;
+        if (c < nch) {
+            float gg[8], bb[8];
+            if (g) unpack8(*reinterpret_cast<const uint4 *>(g + (size_t)c * 8), gg);
+            else for (int e = 0; e < 8; ++e) gg[e] = 1.f;
+            if (b) unpack8(*reinterpret_cast<const uint4 *>(b + (size_t)c * 8), bb);
+            else for (int e = 0; e < 8; ++e) bb[e] = 0.f;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = (v[i][e] - mean) * rstd * gg[e] + bb[e];
+            uint4 o;
+            o.x = pack_bf2(y[0], y[1]);
+            o.y = pack_bf2(y[2], y[3]);
+            o.z = pack_bf2(y[4], y[5]);
+            o.w = pack_bf2(y[6], y[7]);
+            *reinterpret_cast<uint4 *>(dst + (size_t)c * 8) = o;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kLnThreads)
+layernorm_kernel(const uint16_t *x, const uint16_t *g, const uint16_t *b, int h, float eps,
+                 uint16_t *y, int src_stride, const int *last) {
+    __shared__ float red[kLnWarps];
+    const int r = blockIdx.x;
+    const size_t src_row = (size_t)r * src_stride + (last ? last[r] : 0);
+    ln_row(x + src_row * h, g, b, h, eps, y + (size_t)r * h, red);
+}
+
+__global__ void __launch_bounds__(kLnThreads)
+embed_kernel(const int *tokens, const uint16_t *emb, int vocab, const uint16_t *g,
+             const uint16_t *b, int h, float eps, uint16_t *x, const int *len,
+             const int *next_pos, int *pos, int max_seq, int *err) {
+    __shared__ float red[kLnWarps];
+    const int r = blockIdx.x;
+    int tok = tokens[r];
+    if (tok < 0 || tok >= vocab) {
+        if (threadIdx.x == 0) atomicOr(err, kErrToken);
+        tok = 0;
+    }
+    if (len && threadIdx.x == 0) {
+        const int slot = *len;
+        if (slot >= 0 && slot < max_seq) pos[(size_t)r * max_seq + slot] = next_pos[r];
+        else atomicOr(err, kErrSlot);
+    }
+    ln_row(emb + (size_t)tok * h, g, b, h, eps, x + (size_t)r * h, red);
+}
+
+__global__ void slot_pos_kernel(int B, const int *len, const int *next_pos, int *pos,
+                                int max_seq, int *err) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= B) return;
+    const int slot = *len;
+    if (slot >= 0 && slot < max_seq) pos[(size_t)r * max_seq + slot] = next_pos[r];
+    else atomicOr(err, kErrSlot);
+}
+
+// One warp per prompt row: running count of tokens with a ballot scan.
+__global__ void prompt_setup_kernel(const uint8_t *mask, int B, int T, int *pos, int max_seq,
+                                    int *next_pos, int *last, int *len, int *err) {
+    const int r = blockIdx.x;
+    const int lane = threadIdx.x;
+    int count = 0, last_t = -1;
+    for (int t0 = 0; t0 < T; t0 += kWarp) {
+        const int t = t0 + lane;
+        const bool tok = (t < T) && mask[(size_t)r * T + t] != 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, tok);
+        const int before = __popc(bal & ((1u << lane) - 1u));
+        if (t < T) pos[(size_t)r * max_seq + t] = tok ? count + before : -1;
+        count += __popc(bal);
+        if (bal) last_t = t0 + 31 - __clz((int)bal);
+    }
+    if (lane == 0) {
+        next_pos[r] = count;
+        last[r] = last_t < 0 ? T - 1 : last_t;
+        if (count == 0) atomicOr(err, kErrEmptyRow);
+        if (r == 0) *len = T;
+    }
+}
+
+cudaError_t launch_layernorm(const uint16_t *x, const uint16_t *g, const uint16_t *b, int rows,
+                             int h, float eps, uint16_t *y, int src_stride, const int *last,
+                             cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    layernorm_kernel<<<rows, kLnThreads, 0, s>>>(x, g, b, h, eps, y, src_stride, last);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
+                         const uint16_t *g, const uint16_t *b, int h, float eps, uint16_t *x,
+                         const int *len, const int *next_pos, int *pos, int max_seq, int *err,
+                         cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    embed_kernel<<<n, kLnThreads, 0, s>>>(tokens, emb, vocab, g, b, h, eps, x, len, next_pos,
+                                          pos, max_seq, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_slot_pos(int B, const int *len, const int *next_pos, int *pos, int max_seq,
+                            int *err, cudaStream_t s) {
+    slot_pos_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, len, next_pos, pos, max_seq, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prompt_setup(const uint8_t *mask, int B, int T, int *pos, int max_seq,
+                                int *next_pos, int *last, int *len, int *err, cudaStream_t s) {
+    prompt_setup_kernel<<<B, kWarp, 0, s>>>(mask, B, T, pos, max_seq, next_pos, last, len, err);
+    return cudaGetLastError();
+}
+
+}  // namespace bloom

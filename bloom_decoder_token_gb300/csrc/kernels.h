@@ -1,0 +1,101 @@
+// Host-side launch interface of the kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bloom {
+
+constexpr int kMaxBatch = 256;      // largest batch the argmax / decode kernels take
+constexpr int kMaxSplits = 16;      // largest split-KV count
+constexpr int kMaxHidden = 16384;   // LayerNorm register tile bound
+
+enum Epi : int {
+    EPI_STORE = 0,   // out = acc + bias
+    EPI_GELU = 1,    // out = gelu(acc + bias)
+    EPI_RESID = 2,   // out += acc + bias
+    EPI_QKV = 3,     // head-interleaved q | k | v scatter: q -> q_out, k/v -> cache slot
+    EPI_ARGMAX = 4,  // tied LM head: float logits (optional) + fused argmax
+};
+
+struct LinearArgs {
+    const void *w = nullptr;          // bf16 or int8 [N][K]
+    const uint16_t *scale = nullptr;  // bf16 [N] (int8)
+    const uint16_t *bias = nullptr;   // bf16 [N] or null
+    const uint16_t *x = nullptr;      // bf16 [M][K]
+    int M = 0, N = 0, K = 0;
+    int int8 = 0;
+    int epi = EPI_STORE;
+    uint16_t *out = nullptr;          // bf16 [M][N] (STORE / GELU / RESID)
+    // EPI_QKV
+    uint16_t *q_out = nullptr;        // bf16 [M][n_head * d]
+    uint16_t *k_cache = nullptr;      // bf16 [Bkv][n_head][max_seq][d] (this layer)
+    uint16_t *v_cache = nullptr;
+    const int *len_ptr = nullptr;     // decode: slot = *len_ptr
+    int T = 0;                        // prefill: token m is slot m % T of sequence m / T
+    int n_head = 0, head_dim = 0, max_seq = 0;
+    // EPI_ARGMAX
+    float *logits = nullptr;          // float [M][N] or null
+    unsigned long long *best = nullptr;  // [M], zero at rest
+    int *ticket = nullptr;            // zero at rest
+    int *out_tokens = nullptr;        // [M]
+    int *len_inc = nullptr;           // if set: last CTA does ++*len_inc and ++next_pos[m]
+    int *next_pos = nullptr;
+    int *err = nullptr;
+};
+
+cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s);
+cudaError_t linear_prepare();
+
+// LayerNorm of `rows` rows.  Source row r is x[(r * src_stride + (last ? last[r] : 0)) * h].
+cudaError_t launch_layernorm(const uint16_t *x, const uint16_t *g, const uint16_t *b, int rows,
+                             int h, float eps, uint16_t *y, int src_stride, const int *last,
+                             cudaStream_t s);
+
+// Embedding gather + LN for n tokens.  With step state (len != null) it also
+// records the position of slot *len for each of the n sequences.
+cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
+                         const uint16_t *g, const uint16_t *b, int h, float eps, uint16_t *x,
+                         const int *len, const int *next_pos, int *pos, int max_seq, int *err,
+                         cudaStream_t s);
+
+// pos[b][slot=*len] = next_pos[b] for B sequences (layer-level decode entry).
+cudaError_t launch_slot_pos(int B, const int *len, const int *next_pos, int *pos, int max_seq,
+                            int *err, cudaStream_t s);
+
+// Prompt positions: pos[b][t] from the mask cumsum, next_pos[b], last[b] (last
+// token slot), *len = T.
+cudaError_t launch_prompt_setup(const uint8_t *mask, int B, int T, int *pos, int max_seq,
+                                int *next_pos, int *last, int *len, int *err, cudaStream_t s);
+
+struct AttnDecodeArgs {
+    const uint16_t *q = nullptr;     // [B][n][d]
+    const uint16_t *k = nullptr;     // [B][n][max_seq][d]
+    const uint16_t *v = nullptr;
+    const int *pos = nullptr;        // [B][max_seq]
+    const float *slopes = nullptr;   // [n]
+    const int *len_ptr = nullptr;    // keys [0, *len_ptr]; if null, keys [0, len_host]
+    int len_host = 0;
+    int B = 0, n = 0, d = 0, max_seq = 0;
+    int splits = 1;
+    float scale = 0.f;               // 1/sqrt(d)
+    float *part = nullptr;           // [B][n][splits][d + 2]
+    int *ticket = nullptr;           // [B][n], zero at rest
+    uint16_t *o = nullptr;           // [B][n*d]
+};
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s);
+
+struct AttnPrefillArgs {
+    const uint16_t *q = nullptr;     // [B*T][n][d]
+    const uint16_t *k = nullptr;     // [B][n][max_seq][d]
+    const uint16_t *v = nullptr;
+    const int *pos = nullptr;        // [B][max_seq]
+    const float *slopes = nullptr;
+    int B = 0, T = 0, n = 0, d = 0, max_seq = 0;
+    float scale = 0.f;
+    uint16_t *o = nullptr;           // [B*T][n*d]
+};
+cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, cudaStream_t s);
+
+}  // namespace bloom

@@ -1,0 +1,255 @@
+/*
+ * bloom.h -- C ABI of the GB300 (sm_103a) BLOOM decoder engine.
+ *
+ * One job: KV-cached greedy token generation through a BLOOM-architecture
+ * decoder stack on one GPU.  A generation is one prefill of the padded prompts
+ * followed by one decode step per new token, the argmax token fed back in
+ * ("Incredibly Fast BLOOM Inference with DeepSpeed and Accelerate", Benchmark
+ * Environment: greedy, do_sample=False, KV cache enabled; per-token cost =
+ * wall time / (batch x tokens)).
+ *
+ * The block (BLOOM as ported to transformers, "Optimization story: Bloom
+ * inference", Porting to transformers):
+ *   x = LN_emb(E[tok]);  per layer:  a = LN1(x); qkv = Wqkv a + bqkv;
+ *   ALiBi attention with masked keys excluded and a float32 softmax
+ *   ("Hugging Face BLOOM Inference Optimization", Custom CUDA Kernels);
+ *   x += Wo o + bo;  x += Wdown gelu_tanh(Wup LN2(x) + bup) + bdown
+ *   ("Kernel Fusion with torch.jit.script" for the GeLU);
+ *   logits = E LN_f(x) (tied head); next = argmax, lowest index on ties.
+ *
+ * Conventions (all entry points):
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller unless the
+ *    argument says "host".  The library borrows weights for the model's life.
+ *  - Weights use the nn.Linear layout [out][in], row-major, bf16 (IEEE
+ *    binary16-brain) or int8 with one bf16 scale per output row (W = q * s).
+ *    Row pointers of every matrix must be 16-byte aligned (in % 8 == 0 for
+ *    bf16, in % 16 == 0 for int8, base 16-byte aligned).
+ *  - Fused QKV rows are head-interleaved: row (3*j + c)*d + e holds head j,
+ *    c = 0 (query) / 1 (key) / 2 (value), element e, d = hidden / n_head.
+ *  - Calls are asynchronous on the given CUDA stream (a cudaStream_t; NULL =
+ *    the legacy default stream) and return a status validated on the host
+ *    before anything is launched.  A kernel that meets a bad value (a token
+ *    id >= vocab, a slot beyond the cache) records it in a device flag that
+ *    bloom_check_device() reports; kernels never trap.
+ *  - A model is not thread-safe; calls on one model must be issued in order
+ *    on one stream.  Models are independent of one another.
+ */
+#ifndef BLOOM_H
+#define BLOOM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BLOOM_OK = 0,
+    BLOOM_E_INVALID = 1,      /* null / misaligned pointer, bad size or value */
+    BLOOM_E_UNSUPPORTED = 2,  /* shape the kernels do not implement (see bloom_create) */
+    BLOOM_E_OOM = 3,          /* device workspace allocation failed */
+    BLOOM_E_CAPACITY = 4,     /* batch above the cache's, or cache full */
+    BLOOM_E_CUDA = 5,         /* a CUDA runtime call failed; see bloom_last_error() */
+    BLOOM_E_DEVICE_FLAG = 6   /* a kernel recorded a bad value (bloom_check_device) */
+} bloom_status;
+
+enum { BLOOM_WEIGHT_BF16 = 0, BLOOM_WEIGHT_INT8 = 1 };
+
+/* flags */
+enum {
+    BLOOM_FLAG_NO_GRAPH = 1   /* launch decode steps one kernel at a time (debug, profiling) */
+};
+
+typedef struct {
+    int32_t n_layer;
+    int32_t hidden;        /* h; multiple of 256 */
+    int32_t n_head;        /* n; head_dim d = h / n must be 64 or 128 */
+    int32_t ffn;           /* F (4h in BLOOM); multiple of 256 */
+    int32_t vocab;         /* V; the tied embedding has V rows */
+    float   ln_eps;        /* LayerNorm epsilon (1e-5 in BLOOM) */
+    int32_t weight_dtype;  /* BLOOM_WEIGHT_BF16 or BLOOM_WEIGHT_INT8 (block linears only;
+                              the embedding / LM head is always bf16) */
+    int32_t max_batch;     /* largest batch of any call */
+    int32_t max_tokens;    /* largest B*T of any prefill (sizes the activation workspace) */
+    int32_t max_seq;       /* largest cache length (prompt + generated) of any call */
+    int32_t flags;         /* BLOOM_FLAG_* */
+} bloom_config;
+
+/* One linear layer: bf16 weight, or int8 codes + bf16 row scales. */
+typedef struct {
+    const void *w;         /* bf16 [N][K] or int8 [N][K] */
+    const void *scale;     /* bf16 [N] for int8, else NULL */
+    const void *bias;      /* bf16 [N] or NULL (zero bias) */
+} bloom_linear;
+
+typedef struct {
+    const void *ln1_g, *ln1_b;     /* bf16 [h] */
+    bloom_linear qkv;              /* [3h][h] */
+    bloom_linear o;                /* [h][h] */
+    const void *ln2_g, *ln2_b;     /* bf16 [h] */
+    bloom_linear up;               /* [F][h] */
+    bloom_linear down;             /* [h][F] */
+} bloom_layer_weights;
+
+typedef struct {
+    const void *word_emb;          /* bf16 [V][h]; also the tied LM head */
+    const void *emb_ln_g, *emb_ln_b;
+    const void *lnf_g, *lnf_b;
+    const bloom_layer_weights *layers;   /* HOST array [n_layer] of device pointers */
+} bloom_weights;
+
+typedef struct bloom_model bloom_model;   /* opaque */
+
+/* KV cache: one caller-owned device allocation of bloom_kv_bytes() bytes.
+ * Layout (all offsets 256-byte aligned): a 256-byte header (int32 len = slots
+ * filled, shared by all sequences), int32 next_pos[batch] (ALiBi position of
+ * each sequence's next token), int32 pos[batch][max_seq] (position of each
+ * slot, -1 for a pad slot), then K and V, each bf16
+ * [n_layer][batch][n_head][max_seq][d].  The library writes `len` here as a
+ * host mirror of the device counter. */
+typedef struct {
+    void   *buf;
+    size_t  bytes;
+    int32_t batch;
+    int32_t max_seq;
+    int32_t len;
+} bloom_kv;
+
+/* Bytes a cache for `batch` sequences of `max_seq` slots needs (0 on bad args). */
+size_t bloom_kv_bytes(const bloom_config *cfg, int32_t batch, int32_t max_seq);
+
+/* Validate the config and weights, compute the ALiBi slopes once (largest
+ * power of two m <= n heads: 2^(-8i/m), then every other term of the 2m
+ * sequence), allocate the activation workspace, and pick launch shapes.
+ * The current CUDA device is the model's device.  *out is NULL on failure. */
+bloom_status bloom_create(const bloom_config *cfg, const bloom_weights *w, bloom_model **out);
+
+/* Bind `buf` (device, >= bloom_kv_bytes bytes, 256-byte aligned) as an empty
+ * cache and fill *kv.  Clears the header and marks every slot a pad. */
+bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
+                           int32_t batch, int32_t max_seq, void *stream);
+
+/* Prefill: run the B x T padded prompts (tokens int32 [B][T], mask uint8 [B][T],
+ * 1 = token, 0 = pad; each row needs one token), write K,V of slots [0,T),
+ * set slot positions (count of tokens before the slot), and emit the greedy
+ * token of each row's last token slot to out_tokens int32 [B].  out_logits
+ * (float [B][V]) may be NULL.  Requires B == kv->batch, T <= kv->max_seq,
+ * B*T <= max_tokens.  Sets kv->len = T. */
+bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
+                           const uint8_t *mask, int32_t B, int32_t T, int32_t *out_tokens,
+                           float *out_logits, void *stream);
+
+/* One decode step for all kv->batch sequences: next_tokens int32 [B] go to
+ * slot kv->len; out_tokens int32 [B] receives the greedy next token and may
+ * alias next_tokens; out_logits float [B][V] may be NULL.  Unless
+ * BLOOM_FLAG_NO_GRAPH is set, the step is captured once per distinct
+ * (kv, next_tokens, out_tokens, out_logits) into a CUDA graph and replayed.
+ * Increments kv->len; BLOOM_E_CAPACITY once kv->len == kv->max_seq. */
+bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
+                               int32_t *out_tokens, float *out_logits, void *stream);
+
+/* Whole greedy generation with HOST buffers: copies tokens/mask (host int32 /
+ * uint8 [B][T]) to the device, prefills, runs n_new - 1 decode steps feeding
+ * each argmax back on the device, and copies the n_new tokens of every row to
+ * out_host (host int32 [n_new][B]).  Synchronises the stream before returning
+ * and reports a device flag as BLOOM_E_DEVICE_FLAG.  Requires T + n_new - 1
+ * <= kv->max_seq. */
+bloom_status bloom_generate(bloom_model *m, bloom_kv *kv, const int32_t *tokens_host,
+                            const uint8_t *mask_host, int32_t B, int32_t T, int32_t n_new,
+                            int32_t *out_host, void *stream);
+
+/* Synchronise the stream, read and clear the device flag: BLOOM_OK or
+ * BLOOM_E_DEVICE_FLAG (the flag's bits are in bloom_last_error()). */
+bloom_status bloom_check_device(bloom_model *m, void *stream);
+
+/* Free the workspace and graphs.  Caller-owned weights and caches are kept. */
+bloom_status bloom_destroy(bloom_model *m);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *bloom_last_error(void);
+
+/* Kernel launches one decode step issues (for launch accounting). */
+int32_t bloom_decode_launches(const bloom_model *m);
+
+/* ------------------------------------------------------------------------
+ * Layer-level entry points.  They run one piece of the path on caller
+ * buffers, with the same kernels the calls above use; tests use them to feed
+ * each layer a reference input (teacher forcing) and to time one kernel.
+ * ------------------------------------------------------------------------ */
+
+/* One decoder layer of the decode step on x (bf16 [kv->batch][h], in/out) for
+ * the token at slot kv->len: it writes the layer's K,V at that slot and sets
+ * the slot position, but does not advance kv->len. */
+bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
+                                void *stream);
+
+/* Set the slot positions of a prompt (mask uint8 [B][T]) in the cache and
+ * kv->len = T, as the prefill does before its first layer. */
+bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
+                                 int32_t B, int32_t T, void *stream);
+
+/* One decoder layer of the prefill on x (bf16 [B*T][h], in/out), writing K,V
+ * of slots [0,T).  Needs bloom_kv_set_prompt first. */
+bloom_status bloom_layer_prefill(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
+                                 int32_t B, int32_t T, void *stream);
+
+/* Final LayerNorm + tied LM head + argmax on x (bf16 [B][h]): out_tokens int32
+ * [B], out_logits float [B][V] or NULL. */
+bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int32_t *out_tokens,
+                        float *out_logits, void *stream);
+
+/* Tied LM head + argmax alone (one kernel, the model's scratch) on rows that
+ * are already normalised by ln_f: xn bf16 [B][h] -> out_tokens int32 [B],
+ * out_logits float [B][V] or NULL.  Used to time the head in isolation. */
+bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B, int32_t *out_tokens,
+                           float *out_logits, void *stream);
+
+/* Embedding gather + embedding LayerNorm: tokens int32 [n] -> x bf16 [n][h]. */
+bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32_t n, void *x,
+                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * Operator entry points (no model needed), the kernels of the path on raw
+ * buffers.  All bf16 tensors are row-major.
+ * ------------------------------------------------------------------------ */
+
+/* y[r] = LN(x[r]) * g + b over h features, float32 statistics, biased
+ * variance, eps inside the square root; x, y bf16 [rows][h]; g, b bf16 [h]
+ * (NULL: 1 and 0).  h % 8 == 0, h <= 16384. */
+bloom_status bloom_op_layernorm(const void *x, const void *g, const void *b, int32_t rows,
+                                int32_t h, float eps, void *y, void *stream);
+
+enum {
+    BLOOM_EPI_STORE = 0,   /* y = acc + bias */
+    BLOOM_EPI_GELU = 1,    /* y = gelu_tanh(acc + bias) */
+    BLOOM_EPI_RESID = 2    /* y = y + acc + bias (residual add in place) */
+};
+
+/* Weight-streaming linear layer y[M][N] (bf16) = epilogue(x[M][K] W^T + bias)
+ * with float32 accumulation; W per bloom_linear.  K % 8 == 0 (bf16) or
+ * K % 16 == 0 (int8). */
+bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *x, int32_t M,
+                             int32_t N, int32_t K, int32_t epilogue, void *y, void *stream);
+
+/* Split-KV decode attention for one token per sequence.
+ * q bf16 [B][n][d]; k_cache, v_cache bf16 [B][n][max_seq][d]; pos int32
+ * [B][max_seq] (-1 = masked); keys are slots [0, len]; slopes float [n];
+ * o bf16 [B][n*d].  d in {64, 128}.  `splits` key ranges per (b, head), 0 =
+ * library choice. */
+bloom_status bloom_op_attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *pos, const float *slopes, int32_t B,
+                                  int32_t n_head, int32_t d, int32_t max_seq, int32_t len,
+                                  int32_t splits, void *o, void *stream);
+
+/* Tied LM head with fused argmax: logits[m][v] = x[m] . E[v]; out_tokens[m] =
+ * lowest index of the row maximum of the float32 logits; out_logits may be
+ * NULL.  x bf16 [M][K], E bf16 [V][K]. */
+bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, int32_t M, int32_t V,
+                                    int32_t K, int32_t *out_tokens, float *out_logits,
+                                    void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,262 @@
+"""Model-level parity through the C ABI: greedy generation, per-layer teacher
+forcing, graph replay, host-buffer generation, capacity and device-flag errors.
+
+Token decisions: the GPU's token must equal the oracle's argmax wherever the
+oracle's top-2 logit margin exceeds 0.1.  Decode steps are teacher-forced with
+the oracle's tokens so that one low-margin flip cannot derail later steps.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bloom_decoder_token_gb300 as bg
+from bloom_decoder_token_gb300 import synth
+import oracle
+from parity import (assert_kernel_close, assert_stream_close, f64, greedy_agree, max_abs)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def generate_parity(shape, w, steps, tol, flags=0, margin=0.1):
+    """Prefill + `steps` teacher-forced decode steps; returns the max |logit err|."""
+    ids, mask = synth.make_prompts(shape, seed=0)
+    B, T = ids.shape
+    S = T + steps + 1
+    wd = w.to(DEV)
+    gm = bg.Model(wd, max_batch=B, max_tokens=B * T, max_seq=S, flags=flags)
+    kv = gm.new_kv(B, S)
+    om = oracle.Model(w)
+    seqs = om.new_seqs(B, S)
+    lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
+    tok = gm.prefill(kv, ids.to(DEV), mask.to(DEV), logits=lg)
+    ref = om.prefill(seqs, ids.numpy(), mask.numpy())
+    worst = max_abs(lg, ref)
+    assert worst <= tol, f"prefill logits max|err| {worst}"
+    greedy_agree(tok.cpu().numpy(), ref, margin)
+    nxt_d = torch.empty(B, dtype=torch.int32, device=DEV)
+    for s in range(steps):
+        nxt = torch.from_numpy(ref.argmax(axis=1).astype(np.int32))
+        nxt_d.copy_(nxt)
+        tok = gm.decode_step(kv, nxt_d, logits=lg)
+        ref = om.decode(seqs, nxt.numpy())
+        e = max_abs(lg, ref)
+        assert e <= tol, f"decode step {s} logits max|err| {e}"
+        greedy_agree(tok.cpu().numpy(), ref, margin)
+        worst = max(worst, e)
+    gm.check_device()
+    gm.close()
+    return worst
+
+
+# ---------------------------------------------------------------- one block
+@pytest.mark.parametrize("affine", [False, True], ids=["cfg", "random_affine"])
+def test_block_generation(affine):
+    shape = synth.PRESETS["block"]
+    w = synth.make_weights(shape, seed=0, random_affine=affine)
+    generate_parity(shape, w, steps=8, tol=2e-2)
+
+
+def test_block_hidden_states():
+    """Embedding and layer output (bf16 hidden states) within 2e-2, both end to
+    end (GPU embedding -> GPU layer) and teacher-forced (oracle input)."""
+    shape = synth.PRESETS["block"]
+    w = synth.make_weights(shape, seed=0, random_affine=True)
+    ids, mask = synth.make_prompts(shape, seed=0)
+    B, T = ids.shape
+    gm = bg.Model(w.to(DEV), max_batch=B, max_tokens=B * T, max_seq=T + 1)
+    kv = gm.new_kv(B, T + 1)
+    om = oracle.Model(w)
+    seqs = om.new_seqs(B, T + 1)
+    _, taps = om.prefill(seqs, ids.numpy(), mask.numpy(), taps=True)
+    x = gm.embed(ids.reshape(-1).to(DEV))
+    assert_kernel_close(x, taps[0].reshape(B * T, -1), what="embedding")
+    gm.kv_set_prompt(kv, mask.to(DEV))
+    gm.layer_prefill(kv, 0, x, B, T)
+    assert max_abs(x, taps[1].reshape(B * T, -1)) <= 2e-2
+    xt = torch.from_numpy(taps[0].reshape(B * T, -1)).to(torch.bfloat16).to(DEV)
+    gm.layer_prefill(kv, 0, xt, B, T)
+    ref = om.layer_prefill(0, f64(xt.cpu()), mask[0].numpy())
+    assert_stream_close(xt, ref, what="teacher-forced layer")
+    gm.close()
+
+
+# ---------------------------------------------------------------- 560m shape
+def test_560m_shape_generation():
+    shape = synth.PRESETS["560m"]
+    w = synth.make_weights(shape, seed=0)
+    generate_parity(shape, w, steps=3, tol=2e-2)
+
+
+def test_560m_shape_random_affine_two_layers():
+    shape = synth.PRESETS["560m"].with_(n_layer=2)
+    w = synth.make_weights(shape, seed=1, random_affine=True)
+    generate_parity(shape, w, steps=4, tol=2e-2)
+
+
+def test_graph_replay_equals_direct_launches():
+    shape = synth.PRESETS["560m"].with_(n_layer=3, vocab=5000)
+    w = synth.make_weights(shape, seed=2, random_affine=True).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=2)
+    B, T = ids.shape
+    S = T + 6
+    outs = []
+    for flags in (0, bg.FLAG_NO_GRAPH):
+        gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S, flags=flags)
+        kv = gm.new_kv(B, S)
+        lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
+        tok = gm.prefill(kv, ids.to(DEV), mask.to(DEV))
+        hist = [tok.clone()]
+        for _ in range(5):
+            tok = gm.decode_step(kv, tok, tok, logits=lg)   # in-place feedback
+            hist.append(tok.clone())
+        outs.append((torch.stack(hist).cpu(), lg.cpu()))
+        gm.close()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
+def test_generate_host_buffers_matches_steps():
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000)
+    w = synth.make_weights(shape, seed=3, random_affine=True).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=3)
+    B, T = ids.shape
+    n_new = 7
+    S = T + n_new
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S)
+    kv = gm.new_kv(B, S)
+    out = gm.generate(kv, ids.contiguous(), mask.contiguous(), n_new)
+    kv2 = gm.new_kv(B, S)
+    tok = gm.prefill(kv2, ids.to(DEV), mask.to(DEV))
+    hist = [tok.clone()]
+    for _ in range(n_new - 1):
+        tok = gm.decode_step(kv2, tok, tok)
+        hist.append(tok.clone())
+    assert torch.equal(out, torch.stack(hist).cpu())
+    assert kv.len == T + n_new - 1
+    gm.close()
+
+
+def test_capacity_and_device_flag():
+    shape = synth.PRESETS["block"].with_(vocab=512)
+    w = synth.make_weights(shape, seed=4).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=4)
+    B, T = ids.shape
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=T + 2)
+    kv = gm.new_kv(B, T + 2)
+    tok = gm.prefill(kv, ids.to(DEV), mask.to(DEV))
+    tok = gm.decode_step(kv, tok)
+    tok = gm.decode_step(kv, tok)
+    with pytest.raises(bg.BloomError) as ei:
+        gm.decode_step(kv, tok)
+    assert ei.value.status == 4
+    with pytest.raises(bg.BloomError) as ei:
+        gm.new_kv(B + 1, T + 2)
+    assert ei.value.status == 4
+    # a token id outside the vocabulary is recorded, not trapped
+    kv2 = gm.new_kv(B, T + 2)
+    gm.prefill(kv2, ids.to(DEV), mask.to(DEV))
+    bad = torch.full((B,), 10 ** 6, dtype=torch.int32, device=DEV)
+    gm.decode_step(kv2, bad)
+    with pytest.raises(bg.BloomError) as ei:
+        gm.check_device()
+    assert ei.value.status == 6
+    gm.check_device()          # the flag was cleared; the model stays usable
+    gm.decode_step(kv2, tok)
+    gm.check_device()
+    gm.close()
+
+
+def test_empty_prompt_row_is_flagged():
+    shape = synth.PRESETS["block"].with_(vocab=512, batch=2)
+    w = synth.make_weights(shape, seed=5).to(DEV)
+    gm = bg.Model(w, max_batch=2, max_tokens=16, max_seq=9)
+    kv = gm.new_kv(2, 9)
+    ids = torch.zeros(2, 8, dtype=torch.int32, device=DEV)
+    mask = torch.ones(2, 8, dtype=torch.uint8, device=DEV)
+    mask[1] = 0
+    gm.prefill(kv, ids, mask)
+    with pytest.raises(bg.BloomError) as ei:
+        gm.check_device()
+    assert ei.value.status == 6
+    gm.close()
+
+
+# ---------------------------------------------------------------- big shapes, per layer
+def layer_teacher_forced(shape, layers, B, T, seed=0, x_std=(1.0, 8.0)):
+    """Full-size model on the GPU; for each sampled layer, a seeded synthetic
+    residual-stream input goes through the GPU layer and the oracle layer
+    (prefill of T slots, then one decode token), and the logits of a seeded
+    final hidden state go through both heads."""
+    w = synth.make_weights(shape, seed=seed, device=DEV)
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=T + 1)
+    g = torch.Generator(device="cpu").manual_seed(seed + 10)
+    for li, layer in enumerate(layers):
+        sub = synth.Weights(shape, w.word_emb[:1], w.emb_ln_g, w.emb_ln_b, w.lnf_g, w.lnf_b,
+                            [w.layers[layer]])
+        om = oracle.Model(sub)
+        std = x_std[min(li, len(x_std) - 1)]
+        x = (std * torch.randn(B * T, shape.hidden, generator=g)).to(torch.bfloat16)
+        xd = (std * torch.randn(B, shape.hidden, generator=g)).to(torch.bfloat16)
+        mask = torch.ones(B, T, dtype=torch.uint8)
+        mask[0, :min(2, T - 1)] = 0           # left pads on the first row
+        kv = gm.new_kv(B, T + 1)
+        gm.kv_set_prompt(kv, mask.to(DEV))
+        xg = x.to(DEV)
+        gm.layer_prefill(kv, layer, xg, B, T)
+        xdg = xd.to(DEV)
+        gm.layer_decode(kv, layer, xdg)
+        seqs = om.new_seqs(B, T + 1)
+        for b in range(B):
+            ref = om.layer_prefill(0, f64(x[b * T:(b + 1) * T]), mask[b].numpy(), seqs, b)
+            valid = mask[b].numpy().astype(bool)
+            assert_stream_close(xg[b * T:(b + 1) * T][valid], ref[valid],
+                                what=f"layer {layer} prefill row {b}")
+            refd = om.layer_decode(0, f64(xd[b]), seqs, b)
+            assert_stream_close(xdg[b], refd, what=f"layer {layer} decode row {b}")
+        del om, seqs
+    # head on a seeded final hidden state
+    xf = (8.0 * torch.randn(B, shape.hidden, generator=g)).to(torch.bfloat16)
+    lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
+    tok = gm.head(xf.to(DEV), logits=lg)
+    headw = synth.Weights(shape, w.word_emb, w.emb_ln_g, w.emb_ln_b, w.lnf_g, w.lnf_b, [])
+    refl = oracle.Model(headw, n_layer=0).head(f64(xf))
+    assert max_abs(lg, refl) <= 2e-2
+    greedy_agree(tok.cpu().numpy(), refl)
+    gm.close()
+    del w
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_7b1_layers_and_head():
+    layer_teacher_forced(synth.PRESETS["7b1"], [0, 29], B=2, T=16)
+
+
+@pytest.mark.slow
+def test_7b1_int8_layers_and_head():
+    layer_teacher_forced(synth.PRESETS["7b1int8"], [0, 17], B=2, T=16)
+
+
+@pytest.mark.slow
+def test_176b_shape_layer_and_head():
+    layer_teacher_forced(synth.PRESETS["176b14"], [13], B=1, T=8, x_std=(16.0,))
+
+
+@pytest.mark.slow
+def test_7b1_end_to_end_short_prompt():
+    shape = synth.PRESETS["7b1"].with_(prompt=4, batch=1)
+    w = synth.make_weights(shape, seed=0)
+    generate_parity(shape, w, steps=2, tol=2e-2)
