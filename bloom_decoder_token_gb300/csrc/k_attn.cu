@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnDec
 
     const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31;
-    const int nk = (a.len_ptr ? *a.len_ptr : a.len_host) + 1;
+    const int nk = min((a.len_ptr ? *a.len_ptr : a.len_host) + 1, a.max_seq);
     const int chunk = (nk + a.splits - 1) / a.splits;
     const int k0 = split * chunk;
     const int k1 = min(nk, k0 + chunk);
