@@ -258,7 +258,7 @@ class Model:
     def embed(self, tokens, x=None, stream=None):
         n = tokens.numel()
         if x is None:
-            x = torch.empty(n, self.shape.hidden, dtype=torch.bfloat16, device=self.device)
+            x = torch.empty(n, self.shape.hidden, dtype=torch.float32, device=self.device)
         check(lib().bloom_embed(self.h, _p(tokens), n, _p(x), _stream(stream)))
         return x
 

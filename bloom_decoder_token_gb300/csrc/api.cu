@@ -80,8 +80,8 @@ struct bloom_model {
     int d = 0;
     void *ws = nullptr;
     size_t ws_bytes = 0;
-    uint16_t *x = nullptr, *a = nullptr, *q = nullptr, *o = nullptr, *u = nullptr,
-             *xl = nullptr;
+    float *x = nullptr;           // float32 residual stream [max_tokens][h]
+    uint16_t *a = nullptr, *q = nullptr, *o = nullptr, *u = nullptr, *xl = nullptr;
     float *slopes = nullptr;
     unsigned long long *best = nullptr;
     int *head_ticket = nullptr;
@@ -194,7 +194,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     const size_t n = (size_t)cfg->n_head, d = (size_t)m->d;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
-    const size_t o_x = take(MT * h * 2), o_a = take(MT * h * 2), o_q = take(MT * h * 2),
+    const size_t o_x = take(MT * h * 4), o_a = take(MT * h * 2), o_q = take(MT * h * 2),
                  o_o = take(MT * h * 2), o_u = take(MT * F * 2), o_xl = take(MB * h * 2),
                  o_sl = take(n * 4), o_best = take(MB * 8), o_ht = take(4),
                  o_ap = take(MB * n * kMaxSplits * (d + 2) * 4), o_at = take(MB * n * 4),
@@ -209,7 +209,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         return fail(BLOOM_E_OOM, "workspace of %zu bytes: %s", off, cudaGetErrorString(e));
     }
     char *base = (char *)m->ws;
-    m->x = (uint16_t *)(base + o_x);
+    m->x = (float *)(base + o_x);
     m->a = (uint16_t *)(base + o_a);
     m->q = (uint16_t *)(base + o_q);
     m->o = (uint16_t *)(base + o_o);
@@ -317,15 +317,15 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
 // One decoder layer over M tokens.  Decode: M = B sequences, slot *len.
 // Prefill: M = B*T tokens, slots [0, T).
 static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int max_seq, int l,
-                                 int M, int T, int splits, uint16_t *x, cudaStream_t s) {
+                                 int M, int T, int splits, float *x, cudaStream_t s) {
     const bloom_config &c = m->cfg;
     const bloom_layer_weights &L = m->layers[l];
     const int h = c.hidden, F = c.ffn, n = c.n_head, d = m->d;
     const int i8 = c.weight_dtype == BLOOM_WEIGHT_INT8;
     const float eps = c.ln_eps;
     cudaError_t e;
-    if ((e = launch_layernorm(x, (const uint16_t *)L.ln1_g, (const uint16_t *)L.ln1_b, M, h, eps,
-                              m->a, 1, nullptr, s)))
+    if ((e = launch_layernorm_f32(x, (const uint16_t *)L.ln1_g, (const uint16_t *)L.ln1_b, M, h,
+                                  eps, m->a, 1, nullptr, s)))
         return e;
     LinearArgs q = lin_args(L.qkv, i8, m->a, M, 3 * h, h, EPI_QKV);
     q.q_out = m->q;
@@ -372,27 +372,27 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.o = m->o;
         if ((e = launch_attn_prefill(at, s))) return e;
     }
-    LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID);
-    od.out = x;
+    LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID32);
+    od.out32 = x;
     if ((e = launch_linear(od, m->num_sms, s))) return e;
-    if ((e = launch_layernorm(x, (const uint16_t *)L.ln2_g, (const uint16_t *)L.ln2_b, M, h, eps,
-                              m->a, 1, nullptr, s)))
+    if ((e = launch_layernorm_f32(x, (const uint16_t *)L.ln2_g, (const uint16_t *)L.ln2_b, M, h,
+                                  eps, m->a, 1, nullptr, s)))
         return e;
     LinearArgs up = lin_args(L.up, i8, m->a, M, F, h, EPI_GELU);
     up.out = m->u;
     if ((e = launch_linear(up, m->num_sms, s))) return e;
-    LinearArgs dn = lin_args(L.down, i8, m->u, M, h, F, EPI_RESID);
-    dn.out = x;
+    LinearArgs dn = lin_args(L.down, i8, m->u, M, h, F, EPI_RESID32);
+    dn.out32 = x;
     return launch_linear(dn, m->num_sms, s);
 }
 
 // ln_f + tied head + argmax on rows of `x` (row r at x[(r*stride + last[r]) * h]).
-static cudaError_t enqueue_head(bloom_model *m, const uint16_t *x, int B, int stride,
+static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int stride,
                                 const int *last, int32_t *out_tokens, float *logits,
                                 int *len_inc, int *next_pos, cudaStream_t s) {
     const bloom_config &c = m->cfg;
-    cudaError_t e = launch_layernorm(x, (const uint16_t *)m->lnf_g, (const uint16_t *)m->lnf_b, B,
-                                     c.hidden, c.ln_eps, m->xl, stride, last, s);
+    cudaError_t e = launch_layernorm_f32(x, (const uint16_t *)m->lnf_g, (const uint16_t *)m->lnf_b,
+                                         B, c.hidden, c.ln_eps, m->xl, stride, last, s);
     if (e) return e;
     LinearArgs a;
     a.w = m->word_emb;
@@ -561,7 +561,7 @@ extern "C" bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t
     const KvPtrs kp = kv_ptrs(m, kv);
     CK(launch_slot_pos(kv->batch, kp.len, kp.next_pos, kp.pos, kv->max_seq, m->err, s));
     CK(enqueue_layer(m, kp, kv->batch, kv->max_seq, layer, kv->batch, 0,
-                     attn_splits(m, kv->batch, kv->max_seq), (uint16_t *)x, s));
+                     attn_splits(m, kv->batch, kv->max_seq), (float *)x, s));
     return BLOOM_OK;
 }
 
@@ -574,7 +574,7 @@ extern "C" bloom_status bloom_layer_prefill(bloom_model *m, bloom_kv *kv, int32_
     if (B != kv->batch || T < 1 || T > kv->max_seq || (long long)B * T > m->cfg.max_tokens)
         return fail(BLOOM_E_CAPACITY, "B=%d T=%d", B, T);
     const KvPtrs kp = kv_ptrs(m, kv);
-    CK(enqueue_layer(m, kp, B, kv->max_seq, layer, B * T, T, 1, (uint16_t *)x, (cudaStream_t)stream));
+    CK(enqueue_layer(m, kp, B, kv->max_seq, layer, B * T, T, 1, (float *)x, (cudaStream_t)stream));
     return BLOOM_OK;
 }
 
@@ -582,7 +582,7 @@ extern "C" bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int
                                    float *out_logits, void *stream) {
     if (!m || !x || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
     if (B < 1 || B > m->cfg.max_batch) return fail(BLOOM_E_CAPACITY, "B=%d", B);
-    CK(enqueue_head(m, (const uint16_t *)x, B, 1, nullptr, out_tokens, out_logits, nullptr, nullptr,
+    CK(enqueue_head(m, (const float *)x, B, 1, nullptr, out_tokens, out_logits, nullptr, nullptr,
                     (cudaStream_t)stream));
     return BLOOM_OK;
 }
@@ -613,7 +613,7 @@ extern "C" bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32
     if (n < 1) return fail(BLOOM_E_INVALID, "n=%d", n);
     const bloom_config &c = m->cfg;
     CK(launch_embed(tokens, n, (const uint16_t *)m->word_emb, c.vocab, (const uint16_t *)m->emb_ln_g,
-                    (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, (uint16_t *)x, nullptr,
+                    (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, (float *)x, nullptr,
                     nullptr, nullptr, 0, m->err, (cudaStream_t)stream));
     return BLOOM_OK;
 }
@@ -645,10 +645,12 @@ extern "C" bloom_status bloom_op_layernorm(const void *x, const void *g, const v
 extern "C" bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *x,
                                         int32_t M, int32_t N, int32_t K, int32_t epilogue, void *y,
                                         void *stream) {
-    if (!lin || !x || !y) return fail(BLOOM_E_INVALID, "null argument");
+    if (!lin) return fail(BLOOM_E_INVALID, "null argument");
     bloom_status st = check_linear(*lin, int8, N, K, "op", -1);
     if (st) return st;
     if (M < 0 || N < 1) return fail(BLOOM_E_INVALID, "M=%d N=%d", M, N);
+    if (M == 0) return BLOOM_OK;
+    if (!x || !y) return fail(BLOOM_E_INVALID, "null argument");
     if (epilogue < BLOOM_EPI_STORE || epilogue > BLOOM_EPI_RESID)
         return fail(BLOOM_E_INVALID, "epilogue %d", epilogue);
     if (!aligned16(x)) return fail(BLOOM_E_INVALID, "x not 16-byte aligned");

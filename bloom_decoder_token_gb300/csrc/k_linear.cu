@@ -15,7 +15,7 @@
 //    kRows*BT sums finish in kRows*BT - 1 + (5 - log2(kRows*BT)) shuffles
 //    instead of 5 per value (the same goal as SBI-GeMM's cooperative-group
 //    reduction, "DeepSpeed Inference", III.C.2);
-//  * bias, GeLU, the residual add, the head-interleaved Q/K/V scatter into the
+//  * bias, GeLU, the residual add (into the float32 residual stream), the head-interleaved Q/K/V scatter into the
 //    KV cache, and the LM head's argmax are applied in the epilogue (the
 //    fusions of "DeepSpeed Inference", III.D);
 //  * the grid is sized to the SM count and warps loop over (row group, token
@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
             a.out[o] = f2bf(gelu_tanh(v));
         } else if constexpr (EPI == EPI_RESID) {
             a.out[o] = f2bf(bf2f(a.out[o]) + v);
+        } else if constexpr (EPI == EPI_RESID32) {
+            a.out32[o] += v;
         } else if constexpr (EPI == EPI_QKV) {
             const int d = a.head_dim;
             const int j = row / (3 * d);
@@ -245,6 +247,7 @@ static cudaError_t launch_epi(const LinearArgs &a, int num_sms, cudaStream_t s) 
         case EPI_STORE: return launch_t<BT, INT8, EPI_STORE>(a, num_sms, s);
         case EPI_GELU: return launch_t<BT, INT8, EPI_GELU>(a, num_sms, s);
         case EPI_RESID: return launch_t<BT, INT8, EPI_RESID>(a, num_sms, s);
+        case EPI_RESID32: return launch_t<BT, INT8, EPI_RESID32>(a, num_sms, s);
         case EPI_QKV: return launch_t<BT, INT8, EPI_QKV>(a, num_sms, s);
         default: return cudaErrorInvalidValue;
     }
@@ -271,11 +274,13 @@ cudaError_t linear_prepare() {
     prepare_bt<false, EPI_STORE>();
     prepare_bt<false, EPI_GELU>();
     prepare_bt<false, EPI_RESID>();
+    prepare_bt<false, EPI_RESID32>();
     prepare_bt<false, EPI_QKV>();
     prepare_bt<false, EPI_ARGMAX>();
     prepare_bt<true, EPI_STORE>();
     prepare_bt<true, EPI_GELU>();
     prepare_bt<true, EPI_RESID>();
+    prepare_bt<true, EPI_RESID32>();
     prepare_bt<true, EPI_QKV>();
     return cudaGetLastError();
 }

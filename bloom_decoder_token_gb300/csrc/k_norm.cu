@@ -1,5 +1,10 @@
 // LayerNorm, embedding gather + LayerNorm, and the small step-state kernels.
 //
+// The residual stream x is a running sum over layers and is kept in float32
+// (upcasting only the sums and accumulations, as the fused softmax of "Hugging
+// Face BLOOM Inference Optimization" does); LayerNorm reads it and writes the
+// bf16 activations the weight-streaming kernels consume.
+//
 // One CTA normalises one row, all its values held in registers: float32 mean,
 // then float32 biased variance of the deviations (two passes over registers,
 // no E[x^2] - mean^2 cancellation), eps inside the square root, affine gamma /
@@ -15,10 +20,33 @@ constexpr int kLnThreads = 256;
 constexpr int kLnWarps = kLnThreads / kWarp;
 constexpr int kLnChunks = kMaxHidden / 8 / kLnThreads;   // 8-element chunks per thread
 
-__device__ __forceinline__ void ln_row(const uint16_t *__restrict__ src,
+__device__ __forceinline__ void load8(const uint16_t *p, float *f) {
+    unpack8(*reinterpret_cast<const uint4 *>(p), f);
+}
+__device__ __forceinline__ void load8(const float *p, float *f) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0];
+    const float4 b = reinterpret_cast<const float4 *>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(uint16_t *p, const float *y) {
+    uint4 o;
+    o.x = pack_bf2(y[0], y[1]);
+    o.y = pack_bf2(y[2], y[3]);
+    o.z = pack_bf2(y[4], y[5]);
+    o.w = pack_bf2(y[6], y[7]);
+    *reinterpret_cast<uint4 *>(p) = o;
+}
+__device__ __forceinline__ void store8(float *p, const float *y) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
+}
+
+template <typename TIn, typename TOut>
+__device__ __forceinline__ void ln_row(const TIn *__restrict__ src,
                                        const uint16_t *__restrict__ g,
                                        const uint16_t *__restrict__ b, int h, float eps,
-                                       uint16_t *__restrict__ dst, float *red) {
+                                       TOut *__restrict__ dst, float *red) {
     const int nch = h / 8;
     float v[kLnChunks][8];
     float s = 0.f;
@@ -26,7 +54,7 @@ __device__ __forceinline__ void ln_row(const uint16_t *__restrict__ src,
     for (int i = 0; i < kLnChunks; ++i) {
         const int c = threadIdx.x + i * kLnThreads;
         if (c < nch) {
-            unpack8(*reinterpret_cast<const uint4 *>(src + (size_t)c * 8), v[i]);
+            load8(src + (size_t)c * 8, v[i]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) s += v[i][e];
         }
@@ -58,18 +86,14 @@ __device__ __forceinline__ void ln_row(const uint16_t *__restrict__ src,
             float y[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) y[e] = (v[i][e] - mean) * rstd * gg[e] + bb[e];
-            uint4 o;
-            o.x = pack_bf2(y[0], y[1]);
-            o.y = pack_bf2(y[2], y[3]);
-            o.z = pack_bf2(y[4], y[5]);
-            o.w = pack_bf2(y[6], y[7]);
-            *reinterpret_cast<uint4 *>(dst + (size_t)c * 8) = o;
+            store8(dst + (size_t)c * 8, y);
         }
     }
 }
 
+template <typename TIn>
 __global__ void __launch_bounds__(kLnThreads)
-layernorm_kernel(const uint16_t *x, const uint16_t *g, const uint16_t *b, int h, float eps,
+layernorm_kernel(const TIn *x, const uint16_t *g, const uint16_t *b, int h, float eps,
                  uint16_t *y, int src_stride, const int *last) {
     __shared__ float red[kLnWarps];
     const int r = blockIdx.x;
@@ -79,7 +103,7 @@ layernorm_kernel(const uint16_t *x, const uint16_t *g, const uint16_t *b, int h,
 
 __global__ void __launch_bounds__(kLnThreads)
 embed_kernel(const int *tokens, const uint16_t *emb, int vocab, const uint16_t *g,
-             const uint16_t *b, int h, float eps, uint16_t *x, const int *len,
+             const uint16_t *b, int h, float eps, float *x, const int *len,
              const int *next_pos, int *pos, int max_seq, int *err) {
     __shared__ float red[kLnWarps];
     const int r = blockIdx.x;
@@ -132,12 +156,20 @@ cudaError_t launch_layernorm(const uint16_t *x, const uint16_t *g, const uint16_
                              int h, float eps, uint16_t *y, int src_stride, const int *last,
                              cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    layernorm_kernel<<<rows, kLnThreads, 0, s>>>(x, g, b, h, eps, y, src_stride, last);
+    layernorm_kernel<uint16_t><<<rows, kLnThreads, 0, s>>>(x, g, b, h, eps, y, src_stride, last);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_layernorm_f32(const float *x, const uint16_t *g, const uint16_t *b, int rows,
+                                 int h, float eps, uint16_t *y, int src_stride, const int *last,
+                                 cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    layernorm_kernel<float><<<rows, kLnThreads, 0, s>>>(x, g, b, h, eps, y, src_stride, last);
     return cudaGetLastError();
 }
 
 cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
-                         const uint16_t *g, const uint16_t *b, int h, float eps, uint16_t *x,
+                         const uint16_t *g, const uint16_t *b, int h, float eps, float *x,
                          const int *len, const int *next_pos, int *pos, int max_seq, int *err,
                          cudaStream_t s) {
     if (n <= 0) return cudaSuccess;

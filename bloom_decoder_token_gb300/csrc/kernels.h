@@ -17,6 +17,7 @@ enum Epi : int {
     EPI_RESID = 2,   // out += acc + bias
     EPI_QKV = 3,     // head-interleaved q | k | v scatter: q -> q_out, k/v -> cache slot
     EPI_ARGMAX = 4,  // tied LM head: float logits (optional) + fused argmax
+    EPI_RESID32 = 5, // out32 += acc + bias (float32 residual stream)
 };
 
 struct LinearArgs {
@@ -28,6 +29,7 @@ struct LinearArgs {
     int int8 = 0;
     int epi = EPI_STORE;
     uint16_t *out = nullptr;          // bf16 [M][N] (STORE / GELU / RESID)
+    float *out32 = nullptr;           // float [M][N] (RESID32)
     // EPI_QKV
     uint16_t *q_out = nullptr;        // bf16 [M][n_head * d]
     uint16_t *k_cache = nullptr;      // bf16 [Bkv][n_head][max_seq][d] (this layer)
@@ -53,10 +55,14 @@ cudaError_t launch_layernorm(const uint16_t *x, const uint16_t *g, const uint16_
                              int h, float eps, uint16_t *y, int src_stride, const int *last,
                              cudaStream_t s);
 
-// Embedding gather + LN for n tokens.  With step state (len != null) it also
+cudaError_t launch_layernorm_f32(const float *x, const uint16_t *g, const uint16_t *b, int rows,
+                                 int h, float eps, uint16_t *y, int src_stride, const int *last,
+                                 cudaStream_t s);
+
+// Embedding gather + LN for n tokens into the float32 residual stream x.  With step state (len != null) it also
 // records the position of slot *len for each of the n sequences.
 cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
-                         const uint16_t *g, const uint16_t *b, int h, float eps, uint16_t *x,
+                         const uint16_t *g, const uint16_t *b, int h, float eps, float *x,
                          const int *len, const int *next_pos, int *pos, int max_seq, int *err,
                          cudaStream_t s);
 

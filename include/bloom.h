@@ -178,7 +178,10 @@ int32_t bloom_decode_launches(const bloom_model *m);
  * each layer a reference input (teacher forcing) and to time one kernel.
  * ------------------------------------------------------------------------ */
 
-/* One decoder layer of the decode step on x (bf16 [kv->batch][h], in/out) for
+/* The residual stream x of the layer-level calls is float32: it is the running
+ * sum over layers and is kept unrounded; every other activation is bf16. */
+
+/* One decoder layer of the decode step on x (float [kv->batch][h], in/out) for
  * the token at slot kv->len: it writes the layer's K,V at that slot and sets
  * the slot position, but does not advance kv->len. */
 bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
@@ -189,12 +192,12 @@ bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t layer, voi
 bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
                                  int32_t B, int32_t T, void *stream);
 
-/* One decoder layer of the prefill on x (bf16 [B*T][h], in/out), writing K,V
+/* One decoder layer of the prefill on x (float [B*T][h], in/out), writing K,V
  * of slots [0,T).  Needs bloom_kv_set_prompt first. */
 bloom_status bloom_layer_prefill(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
                                  int32_t B, int32_t T, void *stream);
 
-/* Final LayerNorm + tied LM head + argmax on x (bf16 [B][h]): out_tokens int32
+/* Final LayerNorm + tied LM head + argmax on x (float [B][h]): out_tokens int32
  * [B], out_logits float [B][V] or NULL. */
 bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int32_t *out_tokens,
                         float *out_logits, void *stream);
@@ -205,7 +208,7 @@ bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int32_t *out_t
 bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B, int32_t *out_tokens,
                            float *out_logits, void *stream);
 
-/* Embedding gather + embedding LayerNorm: tokens int32 [n] -> x bf16 [n][h]. */
+/* Embedding gather + embedding LayerNorm: tokens int32 [n] -> x float [n][h]. */
 bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32_t n, void *x,
                          void *stream);
 

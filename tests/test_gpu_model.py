@@ -85,9 +85,10 @@ def test_block_hidden_states():
     gm.kv_set_prompt(kv, mask.to(DEV))
     gm.layer_prefill(kv, 0, x, B, T)
     assert max_abs(x, taps[1].reshape(B * T, -1)) <= 2e-2
-    xt = torch.from_numpy(taps[0].reshape(B * T, -1)).to(torch.bfloat16).to(DEV)
-    gm.layer_prefill(kv, 0, xt, B, T)
-    ref = om.layer_prefill(0, f64(xt.cpu()), mask[0].numpy())
+    x_in = torch.from_numpy(taps[0].reshape(B * T, -1)).float()
+    xt = x_in.to(DEV)
+    gm.layer_prefill(kv, 0, xt, B, T)          # in place
+    ref = om.layer_prefill(0, f64(x_in), mask[0].numpy())
     assert_stream_close(xt, ref, what="teacher-forced layer")
     gm.close()
 
@@ -207,8 +208,8 @@ def layer_teacher_forced(shape, layers, B, T, seed=0, x_std=(1.0, 8.0)):
                             [w.layers[layer]])
         om = oracle.Model(sub)
         std = x_std[min(li, len(x_std) - 1)]
-        x = (std * torch.randn(B * T, shape.hidden, generator=g)).to(torch.bfloat16)
-        xd = (std * torch.randn(B, shape.hidden, generator=g)).to(torch.bfloat16)
+        x = (std * torch.randn(B * T, shape.hidden, generator=g)).float()
+        xd = (std * torch.randn(B, shape.hidden, generator=g)).float()
         mask = torch.ones(B, T, dtype=torch.uint8)
         mask[0, :min(2, T - 1)] = 0           # left pads on the first row
         kv = gm.new_kv(B, T + 1)
@@ -221,13 +222,13 @@ def layer_teacher_forced(shape, layers, B, T, seed=0, x_std=(1.0, 8.0)):
         for b in range(B):
             ref = om.layer_prefill(0, f64(x[b * T:(b + 1) * T]), mask[b].numpy(), seqs, b)
             valid = mask[b].numpy().astype(bool)
-            assert_stream_close(xg[b * T:(b + 1) * T][valid], ref[valid],
+            assert_stream_close(f64(xg[b * T:(b + 1) * T])[valid], ref[valid],
                                 what=f"layer {layer} prefill row {b}")
             refd = om.layer_decode(0, f64(xd[b]), seqs, b)
             assert_stream_close(xdg[b], refd, what=f"layer {layer} decode row {b}")
         del om, seqs
     # head on a seeded final hidden state
-    xf = (8.0 * torch.randn(B, shape.hidden, generator=g)).to(torch.bfloat16)
+    xf = (8.0 * torch.randn(B, shape.hidden, generator=g)).float()
     lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
     tok = gm.head(xf.to(DEV), logits=lg)
     headw = synth.Weights(shape, w.word_emb, w.emb_ln_g, w.emb_ln_b, w.lnf_g, w.lnf_b, [])
@@ -258,5 +259,5 @@ def test_176b_shape_layer_and_head():
 @pytest.mark.slow
 def test_7b1_end_to_end_short_prompt():
     shape = synth.PRESETS["7b1"].with_(prompt=4, batch=1)
-    w = synth.make_weights(shape, seed=0)
+    w = synth.make_weights(shape, seed=0, device=DEV)
     generate_parity(shape, w, steps=2, tol=2e-2)
