@@ -207,7 +207,8 @@ def run_ours(args, sh):
     n_new = sh.new_tokens
     S = T + n_new
     w = synth.make_weights(sh, seed=0, device=dev)
-    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S)
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S,
+                  flags=(bg.FLAG_NO_PDL if args.no_pdl else 0))
     kv = gm.new_kv(B, S)
     ids_d, mask_d = ids.to(dev), mask.to(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
@@ -355,6 +356,7 @@ def main():
     ap.add_argument("--cpu-decode-steps", type=int, default=8)
     ap.add_argument("--ref-decode-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--head-traffic", type=float, default=None,
                     help="dram bytes per LM-head launch from an ncu capture of this kernel")
     args = ap.parse_args()

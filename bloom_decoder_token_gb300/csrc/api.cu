@@ -14,6 +14,10 @@
 
 using namespace bloom;
 
+namespace bloom {
+thread_local bool g_pdl = true;
+}
+
 // ----------------------------------------------------------------- errors
 static thread_local std::string g_err;
 
@@ -432,6 +436,7 @@ extern "C" int32_t bloom_decode_launches(const bloom_model *m) {
 
 extern "C" bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
                                             int32_t B, int32_t T, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!mask) return fail(BLOOM_E_INVALID, "null mask");
@@ -447,6 +452,7 @@ extern "C" bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const 
 extern "C" bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
                                       const uint8_t *mask, int32_t B, int32_t T,
                                       int32_t *out_tokens, float *out_logits, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!tokens || !mask || !out_tokens) return fail(BLOOM_E_INVALID, "null tokens/mask/out_tokens");
@@ -470,6 +476,7 @@ extern "C" bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_
 
 extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
                                           int32_t *out_tokens, float *out_logits, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!next_tokens || !out_tokens) return fail(BLOOM_E_INVALID, "null next_tokens/out_tokens");
@@ -552,6 +559,7 @@ extern "C" bloom_status bloom_generate(bloom_model *m, bloom_kv *kv, const int32
 // ----------------------------------------------------------------- layer-level
 extern "C" bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
                                            void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!x) return fail(BLOOM_E_INVALID, "null x");
@@ -567,6 +575,7 @@ extern "C" bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t
 
 extern "C" bloom_status bloom_layer_prefill(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
                                             int32_t B, int32_t T, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!x) return fail(BLOOM_E_INVALID, "null x");
@@ -580,6 +589,7 @@ extern "C" bloom_status bloom_layer_prefill(bloom_model *m, bloom_kv *kv, int32_
 
 extern "C" bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int32_t *out_tokens,
                                    float *out_logits, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     if (!m || !x || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
     if (B < 1 || B > m->cfg.max_batch) return fail(BLOOM_E_CAPACITY, "B=%d", B);
     CK(enqueue_head(m, (const float *)x, B, 1, nullptr, out_tokens, out_logits, nullptr, nullptr,
@@ -589,6 +599,7 @@ extern "C" bloom_status bloom_head(bloom_model *m, const void *x, int32_t B, int
 
 extern "C" bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B,
                                       int32_t *out_tokens, float *out_logits, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     if (!m || !xn || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
     if (B < 1 || B > m->cfg.max_batch) return fail(BLOOM_E_CAPACITY, "B=%d", B);
     if (!aligned16(xn)) return fail(BLOOM_E_INVALID, "xn not 16-byte aligned");
@@ -609,6 +620,7 @@ extern "C" bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B,
 
 extern "C" bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32_t n, void *x,
                                     void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     if (!m || !tokens || !x) return fail(BLOOM_E_INVALID, "null argument");
     if (n < 1) return fail(BLOOM_E_INVALID, "n=%d", n);
     const bloom_config &c = m->cfg;
@@ -633,6 +645,7 @@ static int device_sms() {
 extern "C" bloom_status bloom_op_layernorm(const void *x, const void *g, const void *b,
                                            int32_t rows, int32_t h, float eps, void *y,
                                            void *stream) {
+    g_pdl = true;
     if (!x || !y) return fail(BLOOM_E_INVALID, "null x/y");
     if (rows < 0 || h < 8 || h % 8 || h > kMaxHidden) return fail(BLOOM_E_UNSUPPORTED, "h=%d", h);
     if (!aligned16(x) || !aligned16(y) || (g && !aligned16(g)) || (b && !aligned16(b)))
@@ -645,6 +658,7 @@ extern "C" bloom_status bloom_op_layernorm(const void *x, const void *g, const v
 extern "C" bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *x,
                                         int32_t M, int32_t N, int32_t K, int32_t epilogue, void *y,
                                         void *stream) {
+    g_pdl = true;
     if (!lin) return fail(BLOOM_E_INVALID, "null argument");
     bloom_status st = check_linear(*lin, int8, N, K, "op", -1);
     if (st) return st;
@@ -665,6 +679,7 @@ extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
                                              const float *slopes, int32_t B, int32_t n_head,
                                              int32_t d, int32_t max_seq, int32_t len,
                                              int32_t splits, void *o, void *stream) {
+    g_pdl = true;
     if (!q || !k_cache || !v_cache || !pos || !slopes || !o) return fail(BLOOM_E_INVALID, "null argument");
     if (d != 64 && d != 128) return fail(BLOOM_E_UNSUPPORTED, "d=%d", d);
     if (B < 1 || n_head < 1 || max_seq < 1 || len < 0 || len >= max_seq)
@@ -708,6 +723,7 @@ extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
 extern "C" bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, int32_t M,
                                                int32_t V, int32_t K, int32_t *out_tokens,
                                                float *out_logits, void *stream) {
+    g_pdl = true;
     if (!x || !emb || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
     if (M < 1 || M > kMaxBatch || V < 1 || K < 8 || K % 8)
         return fail(BLOOM_E_UNSUPPORTED, "M=%d V=%d K=%d", M, V, K);

@@ -80,6 +80,11 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return t;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel's results are
+// visible / let the next kernel in the stream start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // tanh-form GeLU with the BLOOM constants; tanhf from the CUDA math library.
 __device__ __forceinline__ float gelu_tanh(float x) {
     return x * 0.5f * (1.0f + tanhf(0.79788456f * x * (1.0f + 0.044715f * x * x)));

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kLnThreads)
 layernorm_kernel(const TIn *x, const uint16_t *g, const uint16_t *b, int h, float eps,
                  uint16_t *y, int src_stride, const int *last) {
     __shared__ float red[kLnWarps];
+    griddep_launch();
+    griddep_wait();
     const int r = blockIdx.x;
     const size_t src_row = (size_t)r * src_stride + (last ? last[r] : 0);
     ln_row(x + src_row * h, g, b, h, eps, y + (size_t)r * h, red);
@@ -106,6 +108,8 @@ embed_kernel(const int *tokens, const uint16_t *emb, int vocab, const uint16_t *
              const uint16_t *b, int h, float eps, float *x, const int *len,
              const int *next_pos, int *pos, int max_seq, int *err) {
     __shared__ float red[kLnWarps];
+    griddep_launch();
+    griddep_wait();
     const int r = blockIdx.x;
     int tok = tokens[r];
     if (tok < 0 || tok >= vocab) {
@@ -122,6 +126,8 @@ embed_kernel(const int *tokens, const uint16_t *emb, int vocab, const uint16_t *
 
 __global__ void slot_pos_kernel(int B, const int *len, const int *next_pos, int *pos,
                                 int max_seq, int *err) {
+    griddep_launch();
+    griddep_wait();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= B) return;
     const int slot = *len;
@@ -132,6 +138,8 @@ __global__ void slot_pos_kernel(int B, const int *len, const int *next_pos, int 
 // One warp per prompt row: running count of tokens with a ballot scan.
 __global__ void prompt_setup_kernel(const uint8_t *mask, int B, int T, int *pos, int max_seq,
                                     int *next_pos, int *last, int *len, int *err) {
+    griddep_launch();
+    griddep_wait();
     const int r = blockIdx.x;
     const int lane = threadIdx.x;
     int count = 0, last_t = -1;
@@ -156,16 +164,16 @@ cudaError_t launch_layernorm(const uint16_t *x, const uint16_t *g, const uint16_
                              int h, float eps, uint16_t *y, int src_stride, const int *last,
                              cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    layernorm_kernel<uint16_t><<<rows, kLnThreads, 0, s>>>(x, g, b, h, eps, y, src_stride, last);
-    return cudaGetLastError();
+    return launch_pdl(layernorm_kernel<uint16_t>, dim3(rows), dim3(kLnThreads), s, x, g, b, h, eps,
+                      y, src_stride, last);
 }
 
 cudaError_t launch_layernorm_f32(const float *x, const uint16_t *g, const uint16_t *b, int rows,
                                  int h, float eps, uint16_t *y, int src_stride, const int *last,
                                  cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    layernorm_kernel<float><<<rows, kLnThreads, 0, s>>>(x, g, b, h, eps, y, src_stride, last);
-    return cudaGetLastError();
+    return launch_pdl(layernorm_kernel<float>, dim3(rows), dim3(kLnThreads), s, x, g, b, h, eps, y,
+                      src_stride, last);
 }
 
 cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
@@ -173,21 +181,20 @@ cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int voca
                          const int *len, const int *next_pos, int *pos, int max_seq, int *err,
                          cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    embed_kernel<<<n, kLnThreads, 0, s>>>(tokens, emb, vocab, g, b, h, eps, x, len, next_pos,
-                                          pos, max_seq, err);
-    return cudaGetLastError();
+    return launch_pdl(embed_kernel, dim3(n), dim3(kLnThreads), s, tokens, emb, vocab, g, b, h, eps,
+                      x, len, next_pos, pos, max_seq, err);
 }
 
 cudaError_t launch_slot_pos(int B, const int *len, const int *next_pos, int *pos, int max_seq,
                             int *err, cudaStream_t s) {
-    slot_pos_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, len, next_pos, pos, max_seq, err);
-    return cudaGetLastError();
+    return launch_pdl(slot_pos_kernel, dim3((B + 127) / 128), dim3(128), s, B, len, next_pos, pos,
+                      max_seq, err);
 }
 
 cudaError_t launch_prompt_setup(const uint8_t *mask, int B, int T, int *pos, int max_seq,
                                 int *next_pos, int *last, int *len, int *err, cudaStream_t s) {
-    prompt_setup_kernel<<<B, kWarp, 0, s>>>(mask, B, T, pos, max_seq, next_pos, last, len, err);
-    return cudaGetLastError();
+    return launch_pdl(prompt_setup_kernel, dim3(B), dim3(kWarp), s, mask, B, T, pos, max_seq,
+                      next_pos, last, len, err);
 }
 
 }  // namespace bloom

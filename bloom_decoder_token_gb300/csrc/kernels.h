@@ -7,6 +7,26 @@
 
 namespace bloom {
 
+// Programmatic dependent launch for every kernel of the path (set per call from
+// the model's flags; BLOOM_FLAG_NO_PDL turns it off).
+extern thread_local bool g_pdl;
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kMaxBatch = 256;      // largest batch the argmax / decode kernels take
 constexpr int kMaxSplits = 16;      // largest split-KV count
 constexpr int kMaxHidden = 16384;   // LayerNorm register tile bound
