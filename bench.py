@@ -208,7 +208,8 @@ def run_ours(args, sh):
     S = T + n_new
     w = synth.make_weights(sh, seed=0, device=dev)
     gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S,
-                  flags=(bg.FLAG_NO_PDL if args.no_pdl else 0))
+                  flags=(bg.FLAG_NO_PDL if args.no_pdl else 0) |
+                  (bg.FLAG_NO_LN_FUSION if args.no_ln_fusion else 0))
     kv = gm.new_kv(B, S)
     ids_d, mask_d = ids.to(dev), mask.to(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
@@ -353,10 +354,12 @@ def main():
     ap.add_argument("--config", default="560m", choices=sorted(synth.PRESETS))
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--new-tokens", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None, help="decoder layers (default: the preset's)")
     ap.add_argument("--cpu-decode-steps", type=int, default=8)
     ap.add_argument("--ref-decode-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--no-ln-fusion", action="store_true", help="separate LayerNorm kernels")
     ap.add_argument("--head-traffic", type=float, default=None,
                     help="dram bytes per LM-head launch from an ncu capture of this kernel")
     args = ap.parse_args()
@@ -367,6 +370,8 @@ def main():
         sh = sh.with_(batch=args.batch)
     if args.new_tokens:
         sh = sh.with_(new_tokens=args.new_tokens)
+    if args.layers:
+        sh = sh.with_(n_layer=args.layers)
     if args.impl == "reference":
         run_reference(args, sh)
     else:

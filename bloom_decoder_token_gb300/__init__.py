@@ -25,6 +25,7 @@ STATUS = {0: "OK", 1: "E_INVALID", 2: "E_UNSUPPORTED", 3: "E_OOM", 4: "E_CAPACIT
 EPI_STORE, EPI_GELU, EPI_RESID = 0, 1, 2
 FLAG_NO_GRAPH = 1
 FLAG_NO_PDL = 2
+FLAG_NO_LN_FUSION = 4
 
 P = C.c_void_p
 I32 = C.c_int32

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbloom.so")
 SOURCES = ["api.cu", "k_linear.cu", "k_norm.cu", "k_attn.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+HEADERS = ["common.cuh", "kernels.h", "tile_ops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

@@ -318,6 +318,21 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
     return a;
 }
 
+// The LayerNorm feeding a linear layer: fused into the persistent kernel's
+// prologue when it applies (decode, shared memory permitting), else one
+// LayerNorm launch writing the bf16 activations the linear layer reads.
+static cudaError_t fused_ln(bloom_model *m, LinearArgs &a, const float *x, const void *g,
+                            const void *b, cudaStream_t s) {
+    a.ln_x = x;
+    a.ln_g = (const uint16_t *)g;
+    a.ln_b = (const uint16_t *)b;
+    a.ln_eps = m->cfg.ln_eps;
+    if (!(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION) && linear_can_fuse_ln(a)) return cudaSuccess;
+    a.ln_x = nullptr;
+    return launch_layernorm_f32(x, (const uint16_t *)g, (const uint16_t *)b, a.M, a.K,
+                                m->cfg.ln_eps, const_cast<uint16_t *>(a.x), 1, nullptr, s);
+}
+
 // One decoder layer over M tokens.  Decode: M = B sequences, slot *len.
 // Prefill: M = B*T tokens, slots [0, T).
 static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int max_seq, int l,
@@ -328,9 +343,6 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     const int i8 = c.weight_dtype == BLOOM_WEIGHT_INT8;
     const float eps = c.ln_eps;
     cudaError_t e;
-    if ((e = launch_layernorm_f32(x, (const uint16_t *)L.ln1_g, (const uint16_t *)L.ln1_b, M, h,
-                                  eps, m->a, 1, nullptr, s)))
-        return e;
     LinearArgs q = lin_args(L.qkv, i8, m->a, M, 3 * h, h, EPI_QKV);
     q.q_out = m->q;
     q.k_cache = kp.k + kp.layer_elems * l;
@@ -341,6 +353,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     q.head_dim = d;
     q.max_seq = max_seq;
     q.err = m->err;
+    if ((e = fused_ln(m, q, x, L.ln1_g, L.ln1_b, s))) return e;
     if ((e = launch_linear(q, m->num_sms, s))) return e;
     if (T == 0) {
         AttnDecodeArgs at;
@@ -378,15 +391,17 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     }
     LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID32);
     od.out32 = x;
+    od.T = T;
     if ((e = launch_linear(od, m->num_sms, s))) return e;
-    if ((e = launch_layernorm_f32(x, (const uint16_t *)L.ln2_g, (const uint16_t *)L.ln2_b, M, h,
-                                  eps, m->a, 1, nullptr, s)))
-        return e;
     LinearArgs up = lin_args(L.up, i8, m->a, M, F, h, EPI_GELU);
     up.out = m->u;
+    up.T = T;
+    if ((e = fused_ln(m, up, x, L.ln2_g, L.ln2_b, s))) return e;
     if ((e = launch_linear(up, m->num_sms, s))) return e;
     LinearArgs dn = lin_args(L.down, i8, m->u, M, h, F, EPI_RESID32);
     dn.out32 = x;
+    dn.T = T;
+    (void)eps;
     return launch_linear(dn, m->num_sms, s);
 }
 
@@ -395,9 +410,6 @@ static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int strid
                                 const int *last, int32_t *out_tokens, float *logits,
                                 int *len_inc, int *next_pos, cudaStream_t s) {
     const bloom_config &c = m->cfg;
-    cudaError_t e = launch_layernorm_f32(x, (const uint16_t *)m->lnf_g, (const uint16_t *)m->lnf_b,
-                                         B, c.hidden, c.ln_eps, m->xl, stride, last, s);
-    if (e) return e;
     LinearArgs a;
     a.w = m->word_emb;
     a.x = m->xl;
@@ -411,6 +423,13 @@ static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int strid
     a.out_tokens = out_tokens;
     a.len_inc = len_inc;
     a.next_pos = next_pos;
+    cudaError_t e;
+    if (stride == 1 && !last) {
+        if ((e = fused_ln(m, a, x, m->lnf_g, m->lnf_b, s))) return e;
+    } else if ((e = launch_layernorm_f32(x, (const uint16_t *)m->lnf_g, (const uint16_t *)m->lnf_b,
+                                         B, c.hidden, c.ln_eps, m->xl, stride, last, s))) {
+        return e;
+    }
     return launch_linear(a, m->num_sms, s);
 }
 
@@ -634,6 +653,7 @@ extern "C" bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32
 static int device_sms() {
     static int sms = 0;
     if (!sms) {
+        linear_prepare();
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -663,14 +683,15 @@ extern "C" bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, c
     bloom_status st = check_linear(*lin, int8, N, K, "op", -1);
     if (st) return st;
     if (M < 0 || N < 1) return fail(BLOOM_E_INVALID, "M=%d N=%d", M, N);
-    if (M == 0) return BLOOM_OK;
-    if (!x || !y) return fail(BLOOM_E_INVALID, "null argument");
     if (epilogue < BLOOM_EPI_STORE || epilogue > BLOOM_EPI_RESID)
         return fail(BLOOM_E_INVALID, "epilogue %d", epilogue);
+    if (M == 0) return BLOOM_OK;
+    if (!x || !y) return fail(BLOOM_E_INVALID, "null argument");
     if (!aligned16(x)) return fail(BLOOM_E_INVALID, "x not 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
     LinearArgs a = lin_args(*lin, int8, (const uint16_t *)x, M, N, K, epilogue);
     a.out = (uint16_t *)y;
-    CK(launch_linear(a, device_sms(), (cudaStream_t)stream));
+    CK(launch_linear(a, device_sms(), s));
     return BLOOM_OK;
 }
 
@@ -730,7 +751,7 @@ extern "C" bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, i
     if (!aligned16(x) || !aligned16(emb)) return fail(BLOOM_E_INVALID, "pointers must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     void *scratch = nullptr;
-    const size_t bytes = 256 + (size_t)M * 8;
+    const size_t bytes = 256 + align256((size_t)M * 8);
     CK(cudaMallocAsync(&scratch, bytes, s));
     cudaError_t e = cudaMemsetAsync(scratch, 0, bytes, s);
     LinearArgs a;

@@ -13,6 +13,7 @@ enum : int {
     kErrToken = 1,      // token id outside [0, vocab)
     kErrSlot = 2,       // cache slot outside [0, max_seq)
     kErrEmptyRow = 4,   // prompt row without a token
+    kErrTimeout = 8,    // a bounded wait expired (results of that launch are invalid)
 };
 
 // ---- bf16 <-> f32 (bf16 is the upper half of a binary32) ----

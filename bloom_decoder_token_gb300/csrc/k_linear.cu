@@ -25,38 +25,23 @@
 //    III.D);
 //  * launched with programmatic stream serialization: the weight loads of the
 //    first tile are issued before griddepcontrol.wait, so they overlap the tail
-//    of the kernel that produces x.
+//    of the kernel that produces x;
+//  * the grid is (row groups x token tiles) / w, w = the fewest waves the SMs
+//    can hold, so every CTA gets w or w - 1 tasks and no partial last wave
+//    leaves SMs idle;
+//  * for one or two decode tokens the input LayerNorm (of the float32 residual)
+//    can be fused: each CTA normalises the rows into shared memory once
+//    ("DeepSpeed Inference", III.D, LN fused with the QKV / intermediate GeMM).
 #include "common.cuh"
 #include "kernels.h"
+#include "tile_ops.cuh"
 
 namespace bloom {
 
 constexpr int kLinWarps = 8;
 constexpr int kLinThreads = kLinWarps * kWarp;
 
-// D[16x8] += A[16x16] * B[16x8], bf16 inputs, float32 accumulators.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Two int8 codes (bytes i, i+1 of w) -> bf16x2, exactly: 2^23 + (q + 128) is an
-// exact float whose low mantissa byte is q + 128; subtracting 2^23 + 128 leaves q.
-__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int i) {
-    const uint32_t b0 = ((w >> (8 * i)) & 0xffu) ^ 0x80u;
-    const uint32_t b1 = ((w >> (8 * i + 8)) & 0xffu) ^ 0x80u;
-    const float f0 = __uint_as_float(0x4b000000u | b0) - 8388736.0f;
-    const float f1 = __uint_as_float(0x4b000000u | b1) - 8388736.0f;
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1), "f"(f0));
-    return r;
-}
-
-template <int MT, bool INT8, int EPI>
+template <int MT, bool INT8, int EPI, bool LNF>
 __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a) {
     constexpr int EPL = INT8 ? 16 : 8;   // weights per lane per chunk (16 bytes)
     constexpr int KC = 4 * EPL;          // k per chunk
@@ -64,8 +49,10 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     constexpr int XW = EPL / 2;          // 32-bit words of x per lane per chunk
     constexpr int U = (MT >= 4) ? 2 : 4; // chunks in flight per warp
 
+    extern __shared__ __align__(16) unsigned char xs[];   // LNF: [M][K*2 + 64] bf16
     __shared__ float red[kLinWarps][MT][4][kWarp];
     __shared__ unsigned long long s_best[EPI == EPI_ARGMAX ? kMaxBatch : 1];
+    __shared__ float s_sum[2 * kLinWarps];
     __shared__ int s_last;
 
     griddep_launch();
@@ -81,7 +68,22 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     const long long tasks = (long long)row_groups * tok_tiles;
     const size_t row_bytes = (size_t)a.K * (INT8 ? 1 : 2);
     const char *wbase = reinterpret_cast<const char *>(a.w);
+    const int PX = a.K * 2 + 64;   // 64 mod 128: two rows' fragments hit disjoint banks
     bool waited = false;
+    if constexpr (LNF) {
+        // pull the first task's weight chunks towards L2 (they depend on no
+        // earlier kernel), then wait for x and normalise its rows once
+        if (blockIdx.x < tasks && q == 0) {
+            const int wrow = (int)(blockIdx.x / tok_tiles) * 8 + g;
+            if (wrow < a.N)
+                for (int c = warp; c < nchunks && c < 2 * U * kLinWarps; c += kLinWarps)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                        wbase + (size_t)wrow * row_bytes + (size_t)c * KC * (INT8 ? 1 : 2)));
+        }
+        griddep_wait();
+        waited = true;
+        layernorm_rows_to_smem(a, xs, PX, s_sum, threadIdx.x, warp, lane);
+    }
 
     for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {
         const int rg = (int)(task / tok_tiles);
@@ -122,8 +124,17 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
 #pragma unroll
                     for (int hh = 0; hh < XW / 4; ++hh) {
                         uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
-                        if (ma < a.M && k < a.K) va = ld_act(a.x + (size_t)ma * a.K + k + 8 * hh);
-                        if (mb < a.M && k < a.K) vb = ld_act(a.x + (size_t)mb * a.K + k + 8 * hh);
+                        if constexpr (LNF) {
+                            if (ma < a.M && k < a.K)
+                                va = *reinterpret_cast<const uint4 *>(xs + (size_t)ma * PX +
+                                                                      (size_t)(k + 8 * hh) * 2);
+                            if (mb < a.M && k < a.K)
+                                vb = *reinterpret_cast<const uint4 *>(xs + (size_t)mb * PX +
+                                                                      (size_t)(k + 8 * hh) * 2);
+                        } else {
+                            if (ma < a.M && k < a.K) va = ld_act(a.x + (size_t)ma * a.K + k + 8 * hh);
+                            if (mb < a.M && k < a.K) vb = ld_act(a.x + (size_t)mb * a.K + k + 8 * hh);
+                        }
                         xa[mt][4 * hh + 0] = va.x; xa[mt][4 * hh + 1] = va.y;
                         xa[mt][4 * hh + 2] = va.z; xa[mt][4 * hh + 3] = va.w;
                         xb[mt][4 * hh + 0] = vb.x; xb[mt][4 * hh + 1] = vb.y;
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
                     }
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
-                        mma_bf16(acc[mt], xa[mt][2 * s], xb[mt][2 * s], xa[mt][2 * s + 1],
+                        mma_bf16_16816(acc[mt], xa[mt][2 * s], xb[mt][2 * s], xa[mt][2 * s + 1],
                                  xb[mt][2 * s + 1], b0, b1);
                 }
             }
@@ -244,81 +255,102 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     }
 }
 
-template <int MT, bool INT8, int EPI>
-static int occupancy() {
-    static int occ = 0;
-    if (occ == 0) {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, linear_kernel<MT, INT8, EPI>,
-                                                          kLinThreads, 0) != cudaSuccess || o < 1)
-            o = 1;
-        occ = o;
+template <int MT, bool INT8, int EPI, bool LNF>
+static int occupancy(size_t smem) {
+    // cached per instance and dynamic shared-memory size (a few sizes per model)
+    static size_t keys[8];
+    static int vals[8];
+    static int n = 0;
+    for (int i = 0; i < n; ++i)
+        if (keys[i] == smem) return vals[i];
+    int o = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, linear_kernel<MT, INT8, EPI, LNF>,
+                                                      kLinThreads, smem) != cudaSuccess || o < 1)
+        o = 1;
+    if (n < 8) {
+        keys[n] = smem;
+        vals[n] = o;
+        ++n;
     }
-    return occ;
+    return o;
 }
 
-template <int MT, bool INT8, int EPI>
+template <int MT, bool INT8, int EPI, bool LNF>
 static cudaError_t launch_t(const LinearArgs &a, int num_sms, cudaStream_t s) {
+    const size_t smem = LNF ? (size_t)a.M * (a.K * 2 + 64) : 0;
     const long long tasks = (long long)((a.N + 7) / 8) * ((a.M + 16 * MT - 1) / (16 * MT));
-    long long blocks = tasks;
-    const long long cap = (long long)num_sms * occupancy<MT, INT8, EPI>();
-    if (blocks > cap) blocks = cap;
+    const long long cap = (long long)num_sms * occupancy<MT, INT8, EPI, LNF>(smem);
+    // the fewest waves the SMs can hold, then just enough CTAs for that many
+    const long long waves = (tasks + cap - 1) / cap;
+    long long blocks = (tasks + waves - 1) / waves;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(linear_kernel<MT, INT8, EPI>, dim3((unsigned)blocks), dim3(kLinThreads), s,
-                      a);
+    return launch_pdl_smem(linear_kernel<MT, INT8, EPI, LNF>, dim3((unsigned)blocks),
+                           dim3(kLinThreads), smem, s, a);
 }
 
-template <int MT, bool INT8>
+template <int MT, bool INT8, bool LNF>
 static cudaError_t launch_epi(const LinearArgs &a, int num_sms, cudaStream_t s) {
     switch (a.epi) {
-        case EPI_STORE: return launch_t<MT, INT8, EPI_STORE>(a, num_sms, s);
-        case EPI_GELU: return launch_t<MT, INT8, EPI_GELU>(a, num_sms, s);
-        case EPI_RESID: return launch_t<MT, INT8, EPI_RESID>(a, num_sms, s);
-        case EPI_RESID32: return launch_t<MT, INT8, EPI_RESID32>(a, num_sms, s);
-        case EPI_QKV: return launch_t<MT, INT8, EPI_QKV>(a, num_sms, s);
+        case EPI_STORE: return launch_t<MT, INT8, EPI_STORE, LNF>(a, num_sms, s);
+        case EPI_GELU: return launch_t<MT, INT8, EPI_GELU, LNF>(a, num_sms, s);
+        case EPI_RESID: return launch_t<MT, INT8, EPI_RESID, LNF>(a, num_sms, s);
+        case EPI_RESID32: return launch_t<MT, INT8, EPI_RESID32, LNF>(a, num_sms, s);
+        case EPI_QKV: return launch_t<MT, INT8, EPI_QKV, LNF>(a, num_sms, s);
+        case EPI_ARGMAX:
+            if constexpr (!INT8) return launch_t<MT, false, EPI_ARGMAX, LNF>(a, num_sms, s);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <bool INT8>
+template <bool INT8, bool LNF>
 static cudaError_t launch_mt(const LinearArgs &a, int num_sms, cudaStream_t s) {
-    if (a.M <= 16) return launch_epi<1, INT8>(a, num_sms, s);
-    if (a.M <= 32) return launch_epi<2, INT8>(a, num_sms, s);
-    return launch_epi<4, INT8>(a, num_sms, s);
+    if (a.M <= 16) return launch_epi<1, INT8, LNF>(a, num_sms, s);
+    if (a.M <= 32) return launch_epi<2, INT8, LNF>(a, num_sms, s);
+    return launch_epi<4, INT8, LNF>(a, num_sms, s);
 }
 
 template <bool INT8, int EPI>
-static void prepare_mt() {
-    occupancy<1, INT8, EPI>();
-    occupancy<2, INT8, EPI>();
-    occupancy<4, INT8, EPI>();
+static cudaError_t prepare_mt() {
+    occupancy<1, INT8, EPI, false>(0);
+    occupancy<2, INT8, EPI, false>(0);
+    occupancy<4, INT8, EPI, false>(0);
+    // only the fused-LayerNorm instance (one token tile) uses dynamic shared memory
+    return cudaFuncSetAttribute(linear_kernel<1, INT8, EPI, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kLnFuseSmemMax);
 }
 
-// Resolve every instance's occupancy once, outside any stream capture.
+// Occupancies and shared-memory limits of every instance, outside any capture.
 cudaError_t linear_prepare() {
-    prepare_mt<false, EPI_STORE>();
-    prepare_mt<false, EPI_GELU>();
-    prepare_mt<false, EPI_RESID>();
-    prepare_mt<false, EPI_RESID32>();
-    prepare_mt<false, EPI_QKV>();
-    prepare_mt<false, EPI_ARGMAX>();
-    prepare_mt<true, EPI_STORE>();
-    prepare_mt<true, EPI_GELU>();
-    prepare_mt<true, EPI_RESID>();
-    prepare_mt<true, EPI_RESID32>();
-    prepare_mt<true, EPI_QKV>();
-    return cudaGetLastError();
+    cudaError_t e;
+    if ((e = prepare_mt<false, EPI_STORE>())) return e;
+    if ((e = prepare_mt<false, EPI_GELU>())) return e;
+    if ((e = prepare_mt<false, EPI_RESID>())) return e;
+    if ((e = prepare_mt<false, EPI_RESID32>())) return e;
+    if ((e = prepare_mt<false, EPI_QKV>())) return e;
+    if ((e = prepare_mt<false, EPI_ARGMAX>())) return e;
+    if ((e = prepare_mt<true, EPI_STORE>())) return e;
+    if ((e = prepare_mt<true, EPI_GELU>())) return e;
+    if ((e = prepare_mt<true, EPI_RESID>())) return e;
+    if ((e = prepare_mt<true, EPI_RESID32>())) return e;
+    return prepare_mt<true, EPI_QKV>();
+}
+
+bool linear_can_fuse_ln(const LinearArgs &a) {
+    return a.T == 0 && a.M >= 1 && a.M <= kLnFuseMaxM &&
+           (size_t)a.M * (a.K * 2 + 64) <= (size_t)kLnFuseSmemMax &&
+           !(a.int8 && a.epi == EPI_ARGMAX);
 }
 
 cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s) {
     if (a.M <= 0 || a.N <= 0) return cudaSuccess;
-    if (a.epi == EPI_ARGMAX) {
-        if (a.int8 || a.M > kMaxBatch) return cudaErrorInvalidValue;
-        if (a.M <= 16) return launch_t<1, false, EPI_ARGMAX>(a, num_sms, s);
-        if (a.M <= 32) return launch_t<2, false, EPI_ARGMAX>(a, num_sms, s);
-        return launch_t<4, false, EPI_ARGMAX>(a, num_sms, s);
+    if (a.epi == EPI_ARGMAX && (a.int8 || a.M > kMaxBatch)) return cudaErrorInvalidValue;
+    if (a.ln_x) {
+        if (!linear_can_fuse_ln(a)) return cudaErrorInvalidValue;
+        return a.int8 ? launch_epi<1, true, true>(a, num_sms, s)
+                      : launch_epi<1, false, true>(a, num_sms, s);
     }
-    return a.int8 ? launch_mt<true>(a, num_sms, s) : launch_mt<false>(a, num_sms, s);
+    return a.int8 ? launch_mt<true, false>(a, num_sms, s) : launch_mt<false, false>(a, num_sms, s);
 }
 
 }  // namespace bloom

@@ -12,6 +12,22 @@ namespace bloom {
 extern thread_local bool g_pdl;
 
 template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_smem(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
                        Args... args) {
     cudaLaunchConfig_t cfg = {};
@@ -30,6 +46,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream
 constexpr int kMaxBatch = 256;      // largest batch the argmax / decode kernels take
 constexpr int kMaxSplits = 16;      // largest split-KV count
 constexpr int kMaxHidden = 16384;   // LayerNorm register tile bound
+constexpr int kLnFuseMaxM = 2;      // fused input LayerNorm: at most this many token rows
+constexpr int kLnFuseSmemMax = kLnFuseMaxM * (2 * kMaxHidden + 64);
 
 enum Epi : int {
     EPI_STORE = 0,   // out = acc + bias
@@ -65,7 +83,15 @@ struct LinearArgs {
     int *len_inc = nullptr;           // if set: last CTA does ++*len_inc and ++next_pos[m]
     int *next_pos = nullptr;
     int *err = nullptr;
+    // fused input LayerNorm (decode, see linear_can_fuse_ln): x = LN(ln_x) with ln_g, ln_b
+    const float *ln_x = nullptr;      // float [M][K] residual rows
+    const uint16_t *ln_g = nullptr, *ln_b = nullptr;
+    float ln_eps = 1e-5f;
 };
+
+// Whether the input LayerNorm can be fused into this linear layer (decode, at
+// most kLnFuseMaxM rows that fit in shared memory).
+bool linear_can_fuse_ln(const LinearArgs &a);
 
 cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s);
 cudaError_t linear_prepare();

@@ -1,0 +1,179 @@
+// Tile-level device helpers of the weight-streaming linear kernels: the
+// mma.sync fragment op, exact int8 -> bf16 widening, the fused epilogues, the
+// LayerNorm prologue into shared memory, and the argmax publication.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bloom {
+
+// D[16x8] += A[16x16] * B[16x8], bf16 inputs, float32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two int8 codes (bytes i, i+1 of w) -> bf16x2, exactly: 2^23 + (q + 128) is an
+// exact float whose low mantissa byte is q + 128; subtracting 2^23 + 128 leaves q,
+// and |q| <= 128 is exact in bf16.
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int i) {
+    const uint32_t b0 = ((w >> (8 * i)) & 0xffu) ^ 0x80u;
+    const uint32_t b1 = ((w >> (8 * i + 8)) & 0xffu) ^ 0x80u;
+    const float f0 = __uint_as_float(0x4b000000u | b0) - 8388736.0f;
+    const float f1 = __uint_as_float(0x4b000000u | b1) - 8388736.0f;
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1), "f"(f0));
+    return r;
+}
+
+// Epilogue of one 16x8 accumulator tile (token rows m_base + g, m_base + g + 8;
+// weight rows row0 + 2q, row0 + 2q + 1), lane = (g, q).  Decode QKV only: the
+// K/V of token m go to slot *len_ptr of sequence m (prefill uses its own path).
+template <bool INT8, int EPI>
+__device__ __forceinline__ void tile_epilogue(const LinearArgs &a, const float (&d)[4],
+                                              int m_base, int row0, int lane,
+                                              unsigned long long *s_best) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int m = m_base + g + 8 * half;
+        if (m >= a.M) continue;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int row = row0 + 2 * q + j;
+            if (row >= a.N) continue;
+            float v = d[2 * half + j];
+            if constexpr (INT8) v *= bf2f(a.scale[row]);
+            if (a.bias) v += bf2f(a.bias[row]);
+            const size_t o = (size_t)m * a.N + row;
+            if constexpr (EPI == EPI_STORE) {
+                a.out[o] = f2bf(v);
+            } else if constexpr (EPI == EPI_GELU) {
+                a.out[o] = f2bf(gelu_tanh(v));
+            } else if constexpr (EPI == EPI_RESID) {
+                a.out[o] = f2bf(bf2f(a.out[o]) + v);
+            } else if constexpr (EPI == EPI_RESID32) {
+                a.out32[o] += v;
+            } else if constexpr (EPI == EPI_QKV) {
+                const int dh = a.head_dim;
+                const int hj = row / (3 * dh);
+                const int cidx = (row / dh) % 3;
+                const int e = row % dh;
+                if (cidx == 0) {
+                    a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e] = f2bf(v);
+                } else {
+                    const int slot = *a.len_ptr;
+                    if (slot >= 0 && slot < a.max_seq) {
+                        uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
+                        cache[(((size_t)m * a.n_head + hj) * a.max_seq + slot) * dh + e] = f2bf(v);
+                    } else if (a.err) {
+                        atomicOr(a.err, kErrSlot);
+                    }
+                }
+            } else if constexpr (EPI == EPI_ARGMAX) {
+                if (a.logits) a.logits[o] = v;
+                atomicMax(&s_best[m], pack_argmax(v, (uint32_t)row));
+            }
+        }
+    }
+}
+
+// LayerNorm of the M float32 rows a.ln_x[M][K] into shared memory as bf16
+// (row pitch px bytes); float32 statistics, biased variance, eps inside the
+// square root.  Rows are spread over the CTA's warps (a team of 256 / rows
+// threads per row, at least one warp); the statistics come from one pass of
+// sums shifted by the row's first element (sum (x-s), sum (x-s)^2), which keeps
+// the variance free of cancellation when |mean| >> std.  All threads of the CTA
+// call it (two barriers).
+__device__ __forceinline__ void layernorm_rows_to_smem(const LinearArgs &a, unsigned char *xs,
+                                                       int px, float *s_sum, int tid, int warp,
+                                                       int lane) {
+    const int nthr = blockDim.x, nw = nthr / 32;
+    int team_w = nw;                        // warps per row
+    while (team_w > 1 && team_w > nw / (a.M < nw ? a.M : nw)) team_w >>= 1;
+    const int teams = nw / team_w;
+    const int team = warp / team_w, tw = warp % team_w;
+    const int tthr = team_w * 32, ttid = tw * 32 + lane;
+    float *stat = s_sum;                    // [nw][2]
+    for (int m0 = 0; m0 < a.M; m0 += teams) {
+        const int m = m0 + team;
+        float s1 = 0.f, s2 = 0.f, shift = 0.f;
+        if (m < a.M) {
+            const float *xr = a.ln_x + (size_t)m * a.K;
+            shift = xr[0];
+            for (int k = ttid * 4; k < a.K; k += 4 * tthr) {
+                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+                const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
+                s1 += (d0 + d1) + (d2 + d3);
+                s2 += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+            }
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        if (lane == 0) {
+            stat[2 * warp] = s1;
+            stat[2 * warp + 1] = s2;
+        }
+        __syncthreads();
+        if (m < a.M) {
+            float t1 = 0.f, t2 = 0.f;
+            for (int w = team * team_w; w < (team + 1) * team_w; ++w) {
+                t1 += stat[2 * w];
+                t2 += stat[2 * w + 1];
+            }
+            const float inv_k = 1.f / (float)a.K;
+            const float dm = t1 * inv_k;
+            const float var = fmaxf(t2 * inv_k - dm * dm, 0.f);
+            const float mean = shift + dm;
+            const float rstd = rsqrtf(var + a.ln_eps);
+            const float *xr = a.ln_x + (size_t)m * a.K;
+            uint16_t *dst = reinterpret_cast<uint16_t *>(xs + (size_t)m * px);
+            for (int k = ttid * 4; k < a.K; k += 4 * tthr) {
+                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+                const uint2 gg = *reinterpret_cast<const uint2 *>(a.ln_g + k);
+                const uint2 bb = *reinterpret_cast<const uint2 *>(a.ln_b + k);
+                uint2 o;
+                o.x = pack_bf2((v.x - mean) * rstd * bf_lo(gg.x) + bf_lo(bb.x),
+                               (v.y - mean) * rstd * bf_hi(gg.x) + bf_hi(bb.x));
+                o.y = pack_bf2((v.z - mean) * rstd * bf_lo(gg.y) + bf_lo(bb.y),
+                               (v.w - mean) * rstd * bf_hi(gg.y) + bf_hi(bb.y));
+                *reinterpret_cast<uint2 *>(dst + k) = o;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// CTA maxima -> global; the last CTA of the grid publishes the tokens and
+// leaves the scratch zeroed for the next launch (no waiting: a ticket decides
+// which CTA is last).  Contains barriers; all threads call it.
+__device__ __forceinline__ void argmax_publish(const LinearArgs &a, unsigned long long *s_best,
+                                               int *s_last, int tid, int grid) {
+    __syncthreads();
+    for (int i = tid; i < a.M; i += blockDim.x)
+        if (s_best[i]) atomicMax(&a.best[i], s_best[i]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *s_last = (atomicAdd(a.ticket, 1) == grid - 1);
+    __syncthreads();
+    if (*s_last) {
+        __threadfence();
+        for (int i = tid; i < a.M; i += blockDim.x) {
+            const unsigned long long p = atomicExch(&a.best[i], 0ull);
+            a.out_tokens[i] = (int)unpack_index(p);
+            if (a.len_inc) a.next_pos[i] += 1;
+        }
+        if (tid == 0) {
+            *a.ticket = 0;
+            if (a.len_inc) *a.len_inc += 1;
+        }
+    }
+}
+
+}  // namespace bloom

@@ -59,8 +59,10 @@ enum { BLOOM_WEIGHT_BF16 = 0, BLOOM_WEIGHT_INT8 = 1 };
 /* flags */
 enum {
     BLOOM_FLAG_NO_GRAPH = 1,  /* launch decode steps one kernel at a time (debug, profiling) */
-    BLOOM_FLAG_NO_PDL = 2     /* launch without programmatic dependent launch (each kernel
+    BLOOM_FLAG_NO_PDL = 2,    /* launch without programmatic dependent launch (each kernel
                                  waits for the previous one to finish before it starts) */
+    BLOOM_FLAG_NO_LN_FUSION = 4  /* run every LayerNorm as its own kernel instead of inside
+                                    the decode linear kernel that consumes it */
 };
 
 typedef struct {

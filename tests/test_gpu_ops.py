@@ -49,7 +49,8 @@ def test_layernorm_constant_row_gives_beta():
 
 # ---------------------------------------------------------------- linear
 SHAPES = [(1, 3072, 1024), (3, 100, 64), (8, 4096, 4096), (5, 13, 16384), (16, 1000, 1024),
-          (33, 50, 512), (2, 4097, 256), (8, 257, 14336)]
+          (33, 50, 512), (2, 4097, 256), (8, 257, 14336), (64, 600, 1040), (1, 40, 57344),
+          (24, 1, 4096), (1, 12288, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -158,7 +159,8 @@ def test_lmhead_argmax(M, V, K):
     x = bf((M, K), g)
     tok, lg = bg.op_lmhead_argmax(x.to(DEV), E.to(DEV))
     ref = oracle.linear(f64(x), oracle.host_bits(E))
-    assert_kernel_close(lg, ref, rel=1e-5, atol_rms=1e-5, what="logits")
+    # float32 logits: accumulation error ~ sqrt(K) * 2^-24 * rms, well under 1e-4 * rms
+    assert_kernel_close(lg, ref, rel=1e-5, atol_rms=1e-4, what="logits")
     lgc = lg.cpu()
     # the token is the lowest index of the maximum of the kernel's own float32 logits
     mx = lgc.max(dim=1, keepdim=True).values
