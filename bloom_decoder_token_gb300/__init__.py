@@ -83,6 +83,7 @@ _SIGS = {
     "bloom_op_linear": (I32, [C.POINTER(Linear), I32, P, I32, I32, I32, I32, P, P]),
     "bloom_op_attn_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P]),
     "bloom_op_lmhead_argmax": (I32, [P, P, I32, I32, I32, P, P, P]),
+    "bloom_op_lmhead_argmax_noalloc": (I32, [P, P, I32, I32, I32, P, P, P]),
 }
 EXPORTS = tuple(_SIGS)
 
@@ -303,4 +304,15 @@ def op_lmhead_argmax(x, emb, logits: bool = True, stream=None):
     lg = torch.empty(M, V, dtype=torch.float32, device=x.device) if logits else None
     check(lib().bloom_op_lmhead_argmax(_p(x), _p(emb), M, V, K, _p(tok), _p(lg),
                                        _stream(stream)))
+    return tok, lg
+
+
+def op_lmhead_argmax_noalloc(x, emb, logits: bool = True, stream=None):
+    """bloom_op_lmhead_argmax without allocation (fixed in-library scratch)."""
+    M, K = x.shape
+    V = emb.shape[0]
+    tok = torch.empty(M, dtype=torch.int32, device=x.device)
+    lg = torch.empty(M, V, dtype=torch.float32, device=x.device) if logits else None
+    check(lib().bloom_op_lmhead_argmax_noalloc(_p(x), _p(emb), M, V, K, _p(tok), _p(lg),
+                                               _stream(stream)))
     return tok, lg

@@ -41,6 +41,15 @@ static bloom_status fail(bloom_status st, const char *fmt, ...) {
 
 extern "C" const char *bloom_last_error(void) { return g_err.c_str(); }
 
+void bloom::bloom_set_error(const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+}
+
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -661,6 +670,8 @@ static int device_sms() {
     }
     return sms;
 }
+
+int bloom::bloom_device_sms() { return device_sms(); }
 
 extern "C" bloom_status bloom_op_layernorm(const void *x, const void *g, const void *b,
                                            int32_t rows, int32_t h, float eps, void *y,

@@ -94,6 +94,11 @@ struct LinearArgs {
 bool linear_can_fuse_ln(const LinearArgs &a);
 
 cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s);
+
+// Library-internal host helpers (defined with the C ABI): set the message of
+// bloom_last_error(), and the SM count of the current device.
+void bloom_set_error(const char *fmt, ...);
+int bloom_device_sms();
 cudaError_t linear_prepare();
 
 // LayerNorm of `rows` rows.  Source row r is x[(r * src_stride + (last ? last[r] : 0)) * h].

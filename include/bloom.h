@@ -256,6 +256,29 @@ bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, int32_t M, i
                                     int32_t K, int32_t *out_tokens, float *out_logits,
                                     void *stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free variant (no counterpart on the pages: an addition of this
+ * library).
+ * ------------------------------------------------------------------------ */
+
+/* Same result as bloom_op_lmhead_argmax, but the call allocates nothing: the
+ * kernel's scratch (a completion ticket and one running maximum per row) is a
+ * fixed array inside the library, present on every GPU that loads it until the
+ * process exits.  For callers that cannot allocate device memory on the call
+ * path (cudaMalloc / cudaFree may synchronise the device or fail under memory
+ * pressure; a framework's caching allocator may own all GPU memory; serving
+ * loops may forbid allocation between requests).
+ *  - M <= 256 rows; larger M returns BLOOM_E_CAPACITY and launches nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *    `stream`) before its kernel; calls whose work overlaps on the GPU (other
+ *    streams, other threads) share the array and race, so serialise them. */
+bloom_status bloom_op_lmhead_argmax_noalloc(const void *x, const void *emb, int32_t M,
+                                            int32_t V, int32_t K, int32_t *out_tokens,
+                                            float *out_logits, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
