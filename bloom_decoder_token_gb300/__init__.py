@@ -26,6 +26,7 @@ EPI_STORE, EPI_GELU, EPI_RESID = 0, 1, 2
 FLAG_NO_GRAPH = 1
 FLAG_NO_PDL = 2
 FLAG_NO_LN_FUSION = 4
+FLAG_NO_TC_GEMM = 8
 
 P = C.c_void_p
 I32 = C.c_int32
@@ -81,6 +82,7 @@ _SIGS = {
     "bloom_embed": (I32, [P, P, I32, P, P]),
     "bloom_op_layernorm": (I32, [P, P, P, I32, I32, C.c_float, P, P]),
     "bloom_op_linear": (I32, [C.POINTER(Linear), I32, P, I32, I32, I32, I32, P, P]),
+    "bloom_op_gemm": (I32, [C.POINTER(Linear), P, I32, I32, I32, I32, P, P]),
     "bloom_op_attn_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P]),
     "bloom_op_lmhead_argmax": (I32, [P, P, I32, I32, I32, P, P, P]),
     "bloom_op_lmhead_argmax_noalloc": (I32, [P, P, I32, I32, I32, P, P, P]),
@@ -284,6 +286,17 @@ def op_linear(x, w=None, bias=None, q=None, scale=None, epilogue=EPI_STORE, y=No
     lin = Linear(_p(w if w is not None else q), _p(scale), _p(bias))
     check(lib().bloom_op_linear(C.byref(lin), 0 if w is not None else 1, _p(x), M, N, K,
                                 epilogue, _p(y), _stream(stream)))
+    return y
+
+
+def op_gemm(x, w, bias=None, epilogue=EPI_STORE, y=None, stream=None):
+    """bf16 linear layer on the tensor-core (tcgen05) GEMM used by prefill."""
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    lin = Linear(_p(w), None, _p(bias))
+    check(lib().bloom_op_gemm(C.byref(lin), _p(x), M, N, K, epilogue, _p(y), _stream(stream)))
     return y
 
 

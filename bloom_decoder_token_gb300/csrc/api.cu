@@ -85,6 +85,13 @@ struct GraphEntry {
     cudaGraphExec_t exec;
 };
 
+// One TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned).
+struct TcMap {
+    alignas(64) unsigned char b[128];
+};
+enum { TC_QKV = 0, TC_O = 1, TC_UP = 2, TC_DOWN = 3, TC_PER_LAYER = 4 };
+enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2 };
+
 struct bloom_model {
     bloom_config cfg;
     const void *word_emb, *emb_ln_g, *emb_ln_b, *lnf_g, *lnf_b;
@@ -108,6 +115,10 @@ struct bloom_model {
     uint8_t *pmask = nullptr;     // [max_tokens]
     cudaStream_t cap = nullptr;
     std::vector<GraphEntry> graphs;
+    // tensor-core prefill GEMM: weight maps [layer][TC_*], activation maps TC_X_*
+    bool tc = false;
+    std::vector<TcMap> wmaps;
+    TcMap xmaps[3];
 };
 
 static int attn_splits(const bloom_model *m, int B, int max_seq) {
@@ -253,6 +264,29 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         linear_prepare() != cudaSuccess) {
         st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
     }
+    // TMA descriptors of every bf16 weight and of the activations the prefill GEMMs read
+    if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_tokens >= kTcMinM) {
+        bool ok = gemm_map_bytes() == sizeof(TcMap);
+        m->wmaps.resize((size_t)cfg->n_layer * TC_PER_LAYER);
+        const int bw = gemm_box_rows_w(), bx = gemm_box_rows_x();
+        for (int l = 0; ok && l < cfg->n_layer; ++l) {
+            const bloom_layer_weights &L = w->layers[l];
+            TcMap *wm = &m->wmaps[(size_t)l * TC_PER_LAYER];
+            ok = gemm_make_map(wm[TC_QKV].b, L.qkv.w, 3 * h, h, bw) &&
+                 gemm_make_map(wm[TC_O].b, L.o.w, h, h, bw) &&
+                 gemm_make_map(wm[TC_UP].b, L.up.w, F, h, bw) &&
+                 gemm_make_map(wm[TC_DOWN].b, L.down.w, h, F, bw);
+        }
+        ok = ok && gemm_make_map(m->xmaps[TC_X_A].b, m->a, (long long)MT, h, bx) &&
+             gemm_make_map(m->xmaps[TC_X_O].b, m->o, (long long)MT, h, bx) &&
+             gemm_make_map(m->xmaps[TC_X_U].b, m->u, (long long)MT, F, bx);
+        if (!ok)
+            st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the prefill GEMM could not be encoded");
+        else if (gemm_prepare() != cudaSuccess)
+            st2 = fail(BLOOM_E_CUDA, "prefill GEMM setup: %s", cudaGetErrorString(cudaGetLastError()));
+        else
+            m->tc = true;
+    }
     if (st2) {
         bloom_destroy(m);
         return st2;
@@ -327,6 +361,15 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
     return a;
 }
 
+// A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
+// kTcMinM tokens or more, else the weight-streaming kernel.
+static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wmap, int xmap,
+                              cudaStream_t s) {
+    if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x)
+        return launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
+    return launch_linear(a, m->num_sms, s);
+}
+
 // The LayerNorm feeding a linear layer: fused into the persistent kernel's
 // prologue when it applies (decode, shared memory permitting), else one
 // LayerNorm launch writing the bf16 activations the linear layer reads.
@@ -363,7 +406,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     q.max_seq = max_seq;
     q.err = m->err;
     if ((e = fused_ln(m, q, x, L.ln1_g, L.ln1_b, s))) return e;
-    if ((e = launch_linear(q, m->num_sms, s))) return e;
+    if ((e = run_linear(m, q, l, TC_QKV, TC_X_A, s))) return e;
     if (T == 0) {
         AttnDecodeArgs at;
         at.q = m->q;
@@ -401,17 +444,17 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID32);
     od.out32 = x;
     od.T = T;
-    if ((e = launch_linear(od, m->num_sms, s))) return e;
+    if ((e = run_linear(m, od, l, TC_O, TC_X_O, s))) return e;
     LinearArgs up = lin_args(L.up, i8, m->a, M, F, h, EPI_GELU);
     up.out = m->u;
     up.T = T;
     if ((e = fused_ln(m, up, x, L.ln2_g, L.ln2_b, s))) return e;
-    if ((e = launch_linear(up, m->num_sms, s))) return e;
+    if ((e = run_linear(m, up, l, TC_UP, TC_X_A, s))) return e;
     LinearArgs dn = lin_args(L.down, i8, m->u, M, h, F, EPI_RESID32);
     dn.out32 = x;
     dn.T = T;
     (void)eps;
-    return launch_linear(dn, m->num_sms, s);
+    return run_linear(m, dn, l, TC_DOWN, TC_X_U, s);
 }
 
 // ln_f + tied head + argmax on rows of `x` (row r at x[(r*stride + last[r]) * h]).
@@ -703,6 +746,32 @@ extern "C" bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, c
     LinearArgs a = lin_args(*lin, int8, (const uint16_t *)x, M, N, K, epilogue);
     a.out = (uint16_t *)y;
     CK(launch_linear(a, device_sms(), s));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, int32_t M,
+                                      int32_t N, int32_t K, int32_t epilogue, void *y,
+                                      void *stream) {
+    g_pdl = true;
+    if (!lin) return fail(BLOOM_E_INVALID, "null argument");
+    bloom_status st = check_linear(*lin, 0, N, K, "op", -1);
+    if (st) return st;
+    if (M < 0 || N < 1) return fail(BLOOM_E_INVALID, "M=%d N=%d", M, N);
+    if (epilogue < BLOOM_EPI_STORE || epilogue > BLOOM_EPI_RESID)
+        return fail(BLOOM_E_INVALID, "epilogue %d", epilogue);
+    if (M == 0) return BLOOM_OK;
+    if (!x || !y) return fail(BLOOM_E_INVALID, "null argument");
+    if (!aligned16(x)) return fail(BLOOM_E_INVALID, "x not 16-byte aligned");
+    device_sms();
+    TcMap mx, mw;
+    if (gemm_map_bytes() != sizeof(TcMap) ||
+        !gemm_make_map(mx.b, x, M, K, gemm_box_rows_x()) ||
+        !gemm_make_map(mw.b, lin->w, N, K, gemm_box_rows_w()))
+        return fail(BLOOM_E_UNSUPPORTED, "TMA descriptors could not be encoded");
+    CK(gemm_prepare());
+    LinearArgs a = lin_args(*lin, 0, (const uint16_t *)x, M, N, K, epilogue);
+    a.out = (uint16_t *)y;
+    CK(launch_gemm_tc(mx.b, mw.b, a, (cudaStream_t)stream));
     return BLOOM_OK;
 }
 

@@ -1,0 +1,417 @@
+// Prefill GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// Y[m][n] = epilogue(sum_k X[m][k] W[n][k]) for the B*T prompt tokens of a
+// prefill: the linear layers there are real dense contractions (compute-bound,
+// "DeepSpeed Inference", III.A / IV.C.1: prompt processing saturates compute),
+// so they run as 128 x 256 output tiles on the tensor cores instead of
+// streaming the weights per token tile.
+//
+// One CTA computes one 128 (tokens) x 256 (features) tile:
+//  * warp 0, one lane: TMA producer.  Two 2-D tensor maps (128B swizzle) move
+//    a 128 x 64 tile of X and a 256 x 64 tile of W per k-block into a 4-stage
+//    shared-memory ring, completing an mbarrier per stage;
+//  * warp 1, one lane: issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32,
+//    M = 128, N = 256, K = 16 per instruction, 4 per k-block) into a TMEM
+//    accumulator of 256 columns, and tcgen05.commit frees each stage when its
+//    MMAs are done; a last commit signals the accumulator complete;
+//  * warps 2-5: epilogue.  Each warp reads its 32-lane quarter of the
+//    accumulator with tcgen05.ld (lane = token row, 32 columns at a time),
+//    adds the bias and applies GeLU, the float32 residual add or the
+//    head-interleaved Q/K/V scatter into the KV cache ("DeepSpeed Inference",
+//    III.D fusions), and stores.
+// Warp 0 also allocates and frees the TMEM columns.  Every wait is bounded
+// (about two seconds of SM clock); on expiry the kernel records kErrTimeout,
+// skips its stores, and still frees TMEM.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bloom {
+
+constexpr int kTcBM = 128;          // tokens per tile (MMA M)
+constexpr int kTcBN = 256;          // features per tile (MMA N)
+constexpr int kTcBK = 64;           // k per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;     // 6 warps
+constexpr int kTcABytes = kTcBM * kTcBK * 2;     // 16 KB
+constexpr int kTcBBytes = kTcBN * kTcBK * 2;     // 32 KB
+constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
+constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 1024;   // + 1 KB alignment slack
+constexpr long long kTcWaitCycles = 4000000000ll;
+
+__device__ __forceinline__ uint32_t tc_smem(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void tc_mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem(bar)), "r"(count));
+}
+__device__ __forceinline__ bool tc_mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(tc_smem(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool tc_mbar_wait(uint64_t *bar, uint32_t parity,
+                                             long long limit = kTcWaitCycles) {
+    if (tc_mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (tc_mbar_test(bar, parity)) return true;
+        if ((i & 15u) == 0 && clock64() - t0 > limit) return false;
+    }
+}
+__device__ __forceinline__ void tc_tma_2d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(tc_smem(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(tc_smem(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row atoms of 1024 bytes (stride 1024),
+// descriptor version 1, swizzle mode 2 (128B).
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3fffu);            // start address
+    d |= (uint64_t)1 << 16;                              // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                    // stride byte offset
+    d |= (uint64_t)1 << 46;                              // version
+    d |= (uint64_t)2 << 61;                              // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            tc_smem(bar))
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Epilogue of 32 consecutive features [nb, nb + 32) of token row m (v = the
+// accumulators); features >= a.N are dropped.
+template <int EPI>
+__device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[32], int m, int nb) {
+    const int nv = min(32, a.N - nb);
+    if (a.bias) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < nv) v[i] += bf2f(a.bias[nb + i]);
+    }
+    if constexpr (EPI == EPI_GELU) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+    }
+    if constexpr (EPI == EPI_RESID32) {
+        float *o = a.out32 + (size_t)m * a.N + nb;
+        if (nv == 32 && ((uintptr_t)o & 15u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 r = *reinterpret_cast<float4 *>(o + i);
+                r.x += v[i];
+                r.y += v[i + 1];
+                r.z += v[i + 2];
+                r.w += v[i + 3];
+                *reinterpret_cast<float4 *>(o + i) = r;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < nv) o[i] += v[i];
+        }
+    } else {
+        uint16_t *o;
+        if constexpr (EPI == EPI_QKV) {
+            // 32 consecutive features lie inside one head's q, k or v (d % 32 == 0)
+            const int dh = a.head_dim;
+            const int hj = nb / (3 * dh);
+            const int cidx = (nb / dh) % 3;
+            const int e0 = nb % dh;
+            if (cidx == 0) {
+                o = a.q_out + (size_t)m * a.n_head * dh + (size_t)hj * dh + e0;
+            } else {
+                const int seq = m / a.T, slot = m - seq * a.T;
+                if (slot >= a.max_seq) {
+                    if (a.err) atomicOr(a.err, kErrSlot);
+                    return;
+                }
+                uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
+                o = cache + (((size_t)seq * a.n_head + hj) * a.max_seq + slot) * dh + e0;
+            }
+        } else {
+            o = a.out + (size_t)m * a.N + nb;
+        }
+        if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < nv) v[i] += bf2f(o[i]);
+        }
+        if (nv == 32 && ((uintptr_t)o & 15u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint4 p;
+                p.x = pack_bf2(v[i], v[i + 1]);
+                p.y = pack_bf2(v[i + 2], v[i + 3]);
+                p.z = pack_bf2(v[i + 4], v[i + 5]);
+                p.w = pack_bf2(v[i + 6], v[i + 7]);
+                *reinterpret_cast<uint4 *>(o + i) = p;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < nv) o[i] = f2bf(v[i]);
+        }
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+               const LinearArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the 128B-swizzled tiles
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        ((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t full[kTcStages], empty[kTcStages], acc_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * kTcBN;
+    const int nkb = (a.K + kTcBK - 1) / kTcBK;
+
+    if (tid == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            tc_mbar_init(&full[s], 1);
+            tc_mbar_init(&empty[s], 1);
+        }
+        tc_mbar_init(&acc_full, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_x) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_w) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         tc_smem(&tmem_base)),
+                     "n"(kTcBN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = tmem_base;
+    griddep_launch();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            griddep_wait();   // X comes from the previous kernel
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kTcStages;
+                const uint32_t par = (uint32_t)((kb / kTcStages) & 1);
+                if (!tc_mbar_wait(&empty[s], par ^ 1u)) {
+                    s_abort = 1;
+                    if (a.err) atomicOr(a.err, kErrTimeout);
+                    break;
+                }
+                unsigned char *sa = smem + (size_t)s * kTcStageBytes;
+                unsigned char *sb = sa + kTcABytes;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                                 tc_smem(&full[s])),
+                             "r"(kTcStageBytes)
+                             : "memory");
+                tc_tma_2d(sa, &tm_x, kb * kTcBK, m0, &full[s]);
+                tc_tma_2d(sb, &tm_w, kb * kTcBK, n0, &full[s]);
+                ++issued;
+            }
+            // no copy of ours may still be landing when the CTA exits
+            for (int i = 0; i < kTcStages && i < issued; ++i) {
+                const int kb = issued - 1 - i;
+                if (!tc_mbar_wait(&full[kb % kTcStages], (uint32_t)((kb / kTcStages) & 1)))
+                    if (a.err) atomicOr(a.err, kErrTimeout);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer
+            constexpr uint32_t idesc = tc_idesc(kTcBM, kTcBN);
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kTcStages;
+                const uint32_t par = (uint32_t)((kb / kTcStages) & 1);
+                if (!tc_mbar_wait(&full[s], par)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t sa = tc_smem(smem + (size_t)s * kTcStageBytes);
+                const uint32_t sb = sa + kTcABytes;
+                const uint64_t da = tc_desc(sa), db = tc_desc(sb);
+#pragma unroll
+                for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes per step
+                    tc_mma(tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+                tc_commit(&empty[s]);   // stage free once these MMAs have read it
+            }
+            if (!ok) {
+                s_abort = 1;
+                if (a.err) atomicOr(a.err, kErrTimeout);
+            }
+            tc_commit(&acc_full);       // accumulator complete (or abandoned)
+        }
+    } else {
+        // ---- epilogue: warps 2..5 -> TMEM lane quarters (warp % 4)
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int m = m0 + row;
+        griddep_wait();   // the residual and the cache belong to earlier kernels too
+        // longer limit than the MMA issuer's, so that its final commit arrives first
+        const bool ok = tc_mbar_wait(&acc_full, 0, 3 * kTcWaitCycles);
+        if (!ok) if (a.err) atomicOr(a.err, kErrTimeout);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const bool store = ok && !*(volatile int *)&s_abort && m < a.M;
+#pragma unroll 1
+        for (int c = 0; c < kTcBN; c += 32) {
+            float v[32];
+            tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);   // whole warp
+            if (store && n0 + c < a.N) tc_store_chunk<EPI>(a, v, m, n0 + c);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "n"(kTcBN));
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map over rows x K (row-major), boxes of box_rows x 64, 128B swizzle.
+bool gemm_make_map(void *map, const void *base, long long rows, long long K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || ((uintptr_t)base & 15u) || (K * 2) % 16) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t gemm_map_bytes() { return sizeof(CUtensorMap); }
+int gemm_box_rows_x() { return kTcBM; }
+int gemm_box_rows_w() { return kTcBN; }
+
+template <int EPI>
+static cudaError_t gemm_launch_t(const void *mx, const void *mw, const LinearArgs &a,
+                                 cudaStream_t s) {
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kTcSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const CUtensorMap &tx = *reinterpret_cast<const CUtensorMap *>(mx);
+    const CUtensorMap &tw = *reinterpret_cast<const CUtensorMap *>(mw);
+    dim3 grid((a.M + kTcBM - 1) / kTcBM, (a.N + kTcBN - 1) / kTcBN);
+    return launch_pdl_smem(gemm_tc_kernel<EPI>, grid, dim3(kTcThreads), kTcSmem, s, tx, tw, a);
+}
+
+cudaError_t gemm_prepare() {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_STORE>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_GELU>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_RESID>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem)))
+        return e;
+    if ((e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_RESID32>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem)))
+        return e;
+    return cudaFuncSetAttribute(gemm_tc_kernel<EPI_QKV>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+}
+
+// X [M][K] and W [N][K] described by maps from gemm_make_map (box rows 128 and
+// 256).  K % 8 == 0; bf16 weights only.
+cudaError_t launch_gemm_tc(const void *map_x, const void *map_w, const LinearArgs &a,
+                           cudaStream_t s) {
+    if (a.M <= 0 || a.N <= 0) return cudaSuccess;
+    if (a.int8 || a.K % 8) return cudaErrorInvalidValue;
+    if (a.epi == EPI_QKV && (a.head_dim % 32 || a.T < 1)) return cudaErrorInvalidValue;
+    switch (a.epi) {
+        case EPI_STORE: return gemm_launch_t<EPI_STORE>(map_x, map_w, a, s);
+        case EPI_GELU: return gemm_launch_t<EPI_GELU>(map_x, map_w, a, s);
+        case EPI_RESID: return gemm_launch_t<EPI_RESID>(map_x, map_w, a, s);
+        case EPI_RESID32: return gemm_launch_t<EPI_RESID32>(map_x, map_w, a, s);
+        case EPI_QKV: return gemm_launch_t<EPI_QKV>(map_x, map_w, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace bloom

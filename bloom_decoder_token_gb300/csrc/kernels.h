@@ -95,6 +95,21 @@ bool linear_can_fuse_ln(const LinearArgs &a);
 
 cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s);
 
+// Tensor-core GEMM (tcgen05 / TMEM / TMA) for prefill-sized M, bf16 weights.
+// A map describes a row-major bf16 [rows][K] matrix for the kernel's TMA loads:
+// gemm_make_map fills gemm_map_bytes() bytes (64-byte aligned storage) and
+// returns false if the driver refuses (base not 16-byte aligned, K % 8 != 0).
+// X maps use box rows gemm_box_rows_x(), W maps gemm_box_rows_w().
+bool gemm_make_map(void *map, const void *base, long long rows, long long K, int box_rows);
+size_t gemm_map_bytes();
+int gemm_box_rows_x();
+int gemm_box_rows_w();
+cudaError_t gemm_prepare();
+// Epilogues STORE / GELU / RESID / RESID32 / QKV (prefill: a.T > 0, d % 32 == 0).
+cudaError_t launch_gemm_tc(const void *map_x, const void *map_w, const LinearArgs &a,
+                           cudaStream_t s);
+constexpr int kTcMinM = 128;        // prefill linears with at least this many tokens use it
+
 // Library-internal host helpers (defined with the C ABI): set the message of
 // bloom_last_error(), and the SM count of the current device.
 void bloom_set_error(const char *fmt, ...);

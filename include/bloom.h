@@ -61,8 +61,10 @@ enum {
     BLOOM_FLAG_NO_GRAPH = 1,  /* launch decode steps one kernel at a time (debug, profiling) */
     BLOOM_FLAG_NO_PDL = 2,    /* launch without programmatic dependent launch (each kernel
                                  waits for the previous one to finish before it starts) */
-    BLOOM_FLAG_NO_LN_FUSION = 4  /* run every LayerNorm as its own kernel instead of inside
+    BLOOM_FLAG_NO_LN_FUSION = 4, /* run every LayerNorm as its own kernel instead of inside
                                     the decode linear kernel that consumes it */
+    BLOOM_FLAG_NO_TC_GEMM = 8    /* prefill linears of >= 128 tokens on the weight-streaming
+                                    kernel instead of the tensor-core (tcgen05) GEMM */
 };
 
 typedef struct {
@@ -238,6 +240,16 @@ enum {
  * K % 16 == 0 (int8). */
 bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *x, int32_t M,
                              int32_t N, int32_t K, int32_t epilogue, void *y, void *stream);
+
+/* The same linear layer on the tensor-core GEMM that prefill uses for batches
+ * of >= 128 tokens ("DeepSpeed Inference", III.A and IV.C.1: prompt processing
+ * is compute-bound): 128 x 256 output tiles, tcgen05.mma into TMEM, operands
+ * moved by TMA.  bf16 weights only (lin->scale must be NULL); x and lin->w
+ * 16-byte aligned; K % 8 == 0; any M >= 0 and N >= 1.  Same epilogues and
+ * result layout as bloom_op_linear.  BLOOM_E_UNSUPPORTED if the driver cannot
+ * describe the operands for TMA. */
+bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, int32_t M, int32_t N,
+                           int32_t K, int32_t epilogue, void *y, void *stream);
 
 /* Split-KV decode attention for one token per sequence.
  * q bf16 [B][n][d]; k_cache, v_cache bf16 [B][n][max_seq][d]; pos int32

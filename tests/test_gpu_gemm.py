@@ -1,0 +1,143 @@
+"""Tensor-core (tcgen05) prefill GEMM against the oracle.
+
+Op level: y = epilogue(x W^T + b) over shapes that span several 128 x 256
+tiles, ragged M / N edges and K tails that are not a multiple of the 64-wide
+k-block.  Model level: prefill batches of >= 128 tokens route their four
+linear layers through this kernel; a teacher-forced layer and a whole
+generation are checked against the oracle, and against the weight-streaming
+path (BLOOM_FLAG_NO_TC_GEMM) for the same inputs.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bloom_decoder_token_gb300 as bg
+from bloom_decoder_token_gb300 import synth
+import oracle
+from parity import assert_kernel_close, assert_stream_close, f64, max_abs
+from test_gpu_model import generate_parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def gen(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def bf(shape, g, std=1.0, mean=0.0):
+    return (torch.randn(shape, generator=g, dtype=torch.float64) * std + mean).to(torch.bfloat16)
+
+
+# (M, N, K): one exact tile; ragged M and N with several k-blocks; K tails of
+# 40 and 8 elements; the 560m QKV / up / down shapes; an N below one tile.
+SHAPES = [(128, 256, 64), (130, 300, 192), (257, 520, 1000), (1, 64, 64), (200, 24, 72),
+          (256, 3072, 1024), (256, 4096, 1024), (256, 1024, 4096), (384, 768, 2056)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("epi", [bg.EPI_STORE, bg.EPI_GELU, bg.EPI_RESID],
+                         ids=["store", "gelu", "resid"])
+def test_gemm(M, N, K, epi):
+    g = gen(M * 7919 + N * 31 + K + epi)
+    W = bf((N, K), g, 0.02)
+    x = bf((M, K), g, 1.0)
+    bias = bf((N,), g, 0.5)
+    y0 = bf((M, N), g, 1.0)
+    acc = oracle.linear(f64(x), oracle.host_bits(W), oracle.host_bits(bias))
+    y = y0.to(DEV).clone()
+    bg.op_gemm(x.to(DEV), W.to(DEV), bias=bias.to(DEV), epilogue=epi, y=y)
+    if epi == bg.EPI_STORE:
+        ref = acc
+    elif epi == bg.EPI_GELU:
+        ref = np.vectorize(oracle.gelu)(acc)
+    else:
+        ref = f64(y0) + acc
+    assert_kernel_close(y, ref, what=f"gemm {M}x{N}x{K}")
+
+
+def test_gemm_no_bias_and_empty():
+    g = gen(3)
+    W = bf((300, 128), g, 0.02)
+    x = bf((140, 128), g)
+    y = bg.op_gemm(x.to(DEV), W.to(DEV))
+    assert_kernel_close(y, oracle.linear(f64(x), oracle.host_bits(W)), what="no bias")
+    e = bg.op_gemm(torch.empty(0, 128, dtype=torch.bfloat16, device=DEV), W.to(DEV))
+    assert e.shape == (0, 300)
+
+
+def test_gemm_matches_streaming_kernel():
+    """Both kernels accumulate the same products in float32: results agree to
+    within a couple of bf16 ulps of the output (only the summation order differs)."""
+    g = gen(11)
+    W = bf((1536, 1024), g, 0.02)
+    x = bf((512, 1024), g)
+    b = bf((1536,), g, 0.5)
+    yt = bg.op_gemm(x.to(DEV), W.to(DEV), bias=b.to(DEV)).float()
+    ys = bg.op_linear(x.to(DEV), w=W.to(DEV), bias=b.to(DEV)).float()
+    tol = 2.0 ** -7 * ys.abs() + 1e-3
+    assert bool(((yt - ys).abs() <= tol).all())
+
+
+# ---------------------------------------------------------------- model level
+def prefill_shape():
+    # one BLOOM-560m-width layer, 4 ragged prompts of 64 tokens: M = 256 prefill rows
+    return synth.PRESETS["block"].with_(batch=4, prompt=64, new_tokens=4, ragged=True)
+
+
+@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_TC_GEMM], ids=["tcgen05", "streaming"])
+def test_prefill_layer_teacher_forced(flags):
+    shape = prefill_shape()
+    w = synth.make_weights(shape, seed=4, random_affine=True)
+    ids, mask = synth.make_prompts(shape, seed=4)
+    B, T = ids.shape
+    gm = bg.Model(w.to(DEV), max_batch=B, max_tokens=B * T, max_seq=T + 1, flags=flags)
+    kv = gm.new_kv(B, T + 1)
+    om = oracle.Model(w)
+    seqs = om.new_seqs(B, T + 1)
+    _, taps = om.prefill(seqs, ids.numpy(), mask.numpy(), taps=True)
+    gm.kv_set_prompt(kv, mask.to(DEV))
+    x_in = torch.from_numpy(taps[0].reshape(B * T, -1)).float()
+    xt = x_in.to(DEV)
+    gm.layer_prefill(kv, 0, xt, B, T)
+    ref = np.concatenate([om.layer_prefill(0, f64(x_in[b * T:(b + 1) * T]), mask[b].numpy())
+                          for b in range(B)])
+    assert_stream_close(xt, ref, what="teacher-forced prefill layer")
+    gm.check_device()
+    gm.close()
+
+
+@pytest.mark.parametrize("affine", [False, True], ids=["cfg", "random_affine"])
+def test_prefill_generation_through_tcgen05(affine):
+    shape = prefill_shape().with_(n_layer=2, vocab=4096)
+    w = synth.make_weights(shape, seed=5, random_affine=affine)
+    generate_parity(shape, w, steps=3, tol=2e-2)
+
+
+def test_prefill_paths_agree():
+    """Greedy tokens and logits of the two prefill paths for the same prompts."""
+    shape = prefill_shape().with_(n_layer=2, vocab=4096)
+    w = synth.make_weights(shape, seed=6).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=6)
+    B, T = ids.shape
+    out = []
+    for flags in (0, bg.FLAG_NO_TC_GEMM):
+        gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=T + 1, flags=flags)
+        kv = gm.new_kv(B, T + 1)
+        lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
+        tok = gm.prefill(kv, ids.to(DEV), mask.to(DEV), logits=lg)
+        gm.check_device()
+        out.append((tok.cpu(), lg.cpu()))
+        gm.close()
+    assert max_abs(out[0][1], out[1][1].double().numpy()) <= 2e-2
