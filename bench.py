@@ -296,7 +296,7 @@ def run_ours(args, sh):
     e2e_value = tokens_all / e2e_s
 
     launches_prefill = 2 + 7 * sh.n_layer + 2
-    launches = args.steps * (launches_prefill + (n_new - 1) * gm.decode_launches)
+    launches = args.steps * (launches_prefill + (n_new - 1) * gm.decode_launches(B))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

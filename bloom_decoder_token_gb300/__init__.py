@@ -27,6 +27,7 @@ FLAG_NO_GRAPH = 1
 FLAG_NO_PDL = 2
 FLAG_NO_LN_FUSION = 4
 FLAG_NO_TC_GEMM = 8
+FLAG_NO_PERSISTENT = 16
 
 P = C.c_void_p
 I32 = C.c_int32
@@ -73,7 +74,7 @@ _SIGS = {
     "bloom_check_device": (I32, [P, P]),
     "bloom_destroy": (I32, [P]),
     "bloom_last_error": (C.c_char_p, []),
-    "bloom_decode_launches": (I32, [P]),
+    "bloom_decode_launches": (I32, [P, I32]),
     "bloom_layer_decode": (I32, [P, C.POINTER(KVC), I32, P, P]),
     "bloom_kv_set_prompt": (I32, [P, C.POINTER(KVC), P, I32, I32, P]),
     "bloom_layer_prefill": (I32, [P, C.POINTER(KVC), I32, P, I32, I32, P]),
@@ -202,9 +203,8 @@ class Model:
         except Exception:
             pass
 
-    @property
-    def decode_launches(self) -> int:
-        return lib().bloom_decode_launches(self.h)
+    def decode_launches(self, batch: int) -> int:
+        return lib().bloom_decode_launches(self.h, batch)
 
     def new_kv(self, batch: int, max_seq: int, stream=None) -> KV:
         return KV(self, batch, max_seq, stream)

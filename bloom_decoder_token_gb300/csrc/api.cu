@@ -92,6 +92,17 @@ struct TcMap {
 enum { TC_QKV = 0, TC_O = 1, TC_UP = 2, TC_DOWN = 3, TC_PER_LAYER = 4 };
 enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2 };
 
+// Phase table of the persistent decode step for one set of step buffers.
+struct PlanEntry {
+    void *kvbuf;
+    const void *next;
+    void *out;
+    void *logits;
+    int B;
+    PersistPhase *phases;   // device copy
+    int n;
+};
+
 struct bloom_model {
     bloom_config cfg;
     const void *word_emb, *emb_ln_g, *emb_ln_b, *lnf_g, *lnf_b;
@@ -119,6 +130,10 @@ struct bloom_model {
     bool tc = false;
     std::vector<TcMap> wmaps;
     TcMap xmaps[3];
+    // persistent decode step: grid (0 = not available), barrier words, phase tables
+    int pgrid = 0;
+    unsigned *pbar = nullptr;
+    std::vector<PlanEntry> plans;
 };
 
 static int attn_splits(const bloom_model *m, int B, int max_seq) {
@@ -169,6 +184,7 @@ extern "C" bloom_status bloom_destroy(bloom_model *m) {
     if (!m) return BLOOM_OK;
     cudaSetDevice(m->dev);
     for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
+    for (auto &p : m->plans) cudaFree(p.phases);
     if (m->cap) cudaStreamDestroy(m->cap);
     if (m->ws) cudaFree(m->ws);
     delete m;
@@ -224,7 +240,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
                  o_ap = take(MB * n * kMaxSplits * (d + 2) * 4), o_at = take(MB * n * 4),
                  o_err = take(4), o_last = take(MB * 4), o_tok = take(MB * 4),
                  o_gen = take((size_t)cfg->max_seq * MB * 4), o_ptok = take(MT * 4),
-                 o_pmask = take(MT);
+                 o_pmask = take(MT), o_pbar = take(16);
     m->ws_bytes = off;
     e = cudaMalloc(&m->ws, m->ws_bytes);
     if (e != cudaSuccess) {
@@ -250,6 +266,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     m->gen = (int32_t *)(base + o_gen);
     m->ptok = (int32_t *)(base + o_ptok);
     m->pmask = (uint8_t *)(base + o_pmask);
+    m->pbar = (unsigned *)(base + o_pbar);
     // ALiBi slopes, once: largest power of two p <= n heads gets 2^(-8i/p),
     // i = 1..p; the remaining heads take 2^(-8i/(2p)) for odd i = 1, 3, ...
     std::vector<float> sl(n);
@@ -263,6 +280,10 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking) != cudaSuccess ||
         linear_prepare() != cudaSuccess) {
         st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    if (!st2 && !(cfg->flags & BLOOM_FLAG_NO_PERSISTENT)) {
+        m->pgrid = persist_grid(i8);   // 0: no cooperative launch of one block per SM here
+        cudaGetLastError();
     }
     // TMA descriptors of every bf16 weight and of the activations the prefill GEMMs read
     if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_tokens >= kTcMinM) {
@@ -501,8 +522,165 @@ static cudaError_t enqueue_decode(bloom_model *m, const bloom_kv *kv, const int3
     return enqueue_head(m, m->x, B, 1, nullptr, out, logits, kp.len, kp.next_pos, s);
 }
 
-extern "C" int32_t bloom_decode_launches(const bloom_model *m) {
-    return m ? 1 + 7 * m->cfg.n_layer + 2 : 0;
+static bool use_persistent(const bloom_model *m, int B) {
+    return m->pgrid > 0 && B >= 1 && B <= kPersistMaxM;
+}
+
+extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
+    if (!m) return 0;
+    return use_persistent(m, batch) ? 1 : 1 + 7 * m->cfg.n_layer + 2;
+}
+
+// Key ranges per (sequence, head) in the persistent step: one visit of every
+// block covers all units.
+static int persist_splits(const bloom_model *m, int B, int max_seq) {
+    int s = m->pgrid / (B * m->cfg.n_head);
+    const int cap = (max_seq + 31) / 32;
+    if (s > cap) s = cap;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return s < 1 ? 1 : s;
+}
+
+// The persistent step's phases: embedding; per layer LN1, QKV (+ K/V append),
+// attention, dense (+ residual), LN2, up (+ GeLU), down (+ residual); ln_f;
+// LM head + argmax.  The same operations and buffers as the per-launch step.
+static std::vector<PersistPhase> persist_plan(bloom_model *m, const bloom_kv *kv,
+                                              const int32_t *next, int32_t *out, float *logits) {
+    const bloom_config &c = m->cfg;
+    const KvPtrs kp = kv_ptrs(m, kv);
+    const int B = kv->batch, h = c.hidden, F = c.ffn, n = c.n_head, d = m->d;
+    const int i8 = c.weight_dtype == BLOOM_WEIGHT_INT8;
+    std::vector<PersistPhase> v;
+    PersistPhase e;
+    e.kind = PH_EMBED;
+    e.rows = B;
+    e.h = h;
+    e.eps = c.ln_eps;
+    e.g = (const uint16_t *)m->emb_ln_g;
+    e.b = (const uint16_t *)m->emb_ln_b;
+    e.tokens = next;
+    e.emb = (const uint16_t *)m->word_emb;
+    e.vocab = c.vocab;
+    e.emb_dst = m->x;
+    e.len = kp.len;
+    e.next_pos = kp.next_pos;
+    e.pos = kp.pos;
+    e.max_seq = kv->max_seq;
+    v.push_back(e);
+    auto ln = [&](const void *g, const void *b, uint16_t *dst) {
+        PersistPhase p;
+        p.kind = PH_LN;
+        p.rows = B;
+        p.h = h;
+        p.eps = c.ln_eps;
+        p.g = (const uint16_t *)g;
+        p.b = (const uint16_t *)b;
+        p.ln_src = m->x;
+        p.ln_dst = dst;
+        v.push_back(p);
+    };
+    auto lin = [&](const LinearArgs &a) {
+        PersistPhase p;
+        p.kind = PH_LINEAR;
+        p.lin = a;
+        persist_linear_geometry(p);
+        v.push_back(p);
+    };
+    const int splits = persist_splits(m, B, kv->max_seq);
+    for (int l = 0; l < c.n_layer; ++l) {
+        const bloom_layer_weights &L = m->layers[l];
+        ln(L.ln1_g, L.ln1_b, m->a);
+        LinearArgs q = lin_args(L.qkv, i8, m->a, B, 3 * h, h, EPI_QKV);
+        q.q_out = m->q;
+        q.k_cache = kp.k + kp.layer_elems * l;
+        q.v_cache = kp.v + kp.layer_elems * l;
+        q.len_ptr = kp.len;
+        q.n_head = n;
+        q.head_dim = d;
+        q.max_seq = kv->max_seq;
+        q.err = m->err;
+        lin(q);
+        PersistPhase at;
+        at.kind = PH_ATTN;
+        at.at.q = m->q;
+        at.at.k = q.k_cache;
+        at.at.v = q.v_cache;
+        at.at.pos = kp.pos;
+        at.at.slopes = m->slopes;
+        at.at.len_ptr = kp.len;
+        at.at.B = B;
+        at.at.n = n;
+        at.at.d = d;
+        at.at.max_seq = kv->max_seq;
+        at.at.splits = splits;
+        at.at.scale = (float)(1.0 / sqrt((double)d));
+        at.at.part = m->attn_part;
+        at.at.ticket = m->attn_ticket;
+        at.at.o = m->o;
+        v.push_back(at);
+        LinearArgs od = lin_args(L.o, i8, m->o, B, h, h, EPI_RESID32);
+        od.out32 = m->x;
+        lin(od);
+        ln(L.ln2_g, L.ln2_b, m->a);
+        LinearArgs up = lin_args(L.up, i8, m->a, B, F, h, EPI_GELU);
+        up.out = m->u;
+        lin(up);
+        LinearArgs dn = lin_args(L.down, i8, m->u, B, h, F, EPI_RESID32);
+        dn.out32 = m->x;
+        lin(dn);
+    }
+    ln(m->lnf_g, m->lnf_b, m->xl);
+    LinearArgs hd;
+    hd.w = m->word_emb;
+    hd.x = m->xl;
+    hd.M = B;
+    hd.N = c.vocab;
+    hd.K = h;
+    hd.epi = EPI_ARGMAX;
+    hd.logits = logits;
+    hd.best = m->best;
+    hd.ticket = m->head_ticket;
+    hd.out_tokens = out;
+    hd.len_inc = kp.len;
+    hd.next_pos = kp.next_pos;
+    lin(hd);
+    return v;
+}
+
+static bloom_status decode_persistent(bloom_model *m, const bloom_kv *kv, const int32_t *next,
+                                      int32_t *out, float *logits, cudaStream_t s) {
+    PlanEntry *pe = nullptr;
+    for (auto &p : m->plans)
+        if (p.kvbuf == kv->buf && p.next == next && p.out == out && p.logits == logits &&
+            p.B == kv->batch) {
+            pe = &p;
+            break;
+        }
+    if (!pe) {
+        const std::vector<PersistPhase> v = persist_plan(m, kv, next, out, logits);
+        PersistPhase *d = nullptr;
+        CK(cudaMalloc(&d, v.size() * sizeof(PersistPhase)));
+        cudaError_t e = cudaMemcpyAsync(d, v.data(), v.size() * sizeof(PersistPhase),
+                                        cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // v is freed on return
+        if (e != cudaSuccess) {
+            cudaFree(d);
+            return fail(BLOOM_E_CUDA, "phase table: %s", cudaGetErrorString(e));
+        }
+        if (m->plans.size() >= 16) {
+            cudaFree(m->plans.front().phases);
+            m->plans.erase(m->plans.begin());
+        }
+        m->plans.push_back({kv->buf, next, out, logits, kv->batch, d, (int)v.size()});
+        pe = &m->plans.back();
+    }
+    PersistArgs pa;
+    pa.phases = pe->phases;
+    pa.nphases = pe->n;
+    pa.bar = m->pbar;
+    pa.err = m->err;
+    CK(launch_decode_persistent(pa, m->cfg.weight_dtype == BLOOM_WEIGHT_INT8, m->pgrid, s));
+    return BLOOM_OK;
 }
 
 extern "C" bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
@@ -554,7 +732,9 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
     if (kv->len < 1) return fail(BLOOM_E_INVALID, "decode before prefill");
     if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full (%d slots)", kv->max_seq);
     cudaStream_t s = (cudaStream_t)stream;
-    if (m->cfg.flags & BLOOM_FLAG_NO_GRAPH) {
+    if (use_persistent(m, kv->batch)) {
+        if ((st = decode_persistent(m, kv, next_tokens, out_tokens, out_logits, s))) return st;
+    } else if (m->cfg.flags & BLOOM_FLAG_NO_GRAPH) {
         CK(enqueue_decode(m, kv, next_tokens, out_tokens, out_logits, s));
     } else {
         cudaGraphExec_t exec = nullptr;
@@ -598,7 +778,8 @@ extern "C" bloom_status bloom_check_device(bloom_model *m, void *stream) {
     CK(cudaStreamSynchronize(s));
     if (flag)
         return fail(BLOOM_E_DEVICE_FLAG, "device flag 0x%x (1: token id out of range, 2: cache "
-                    "slot out of range, 4: prompt row without a token)", flag);
+                    "slot out of range, 4: prompt row without a token, 8: a bounded device wait "
+                    "expired)", flag);
     return BLOOM_OK;
 }
 

@@ -170,4 +170,50 @@ struct AttnPrefillArgs {
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, cudaStream_t s);
 
+// ---- persistent decode step (one cooperative launch per step) ----
+enum PhaseKind : int {
+    PH_EMBED = 0,    // embedding gather + LN of the step's tokens -> float32 rows
+    PH_LN = 1,       // LayerNorm of float32 rows -> bf16 rows
+    PH_LINEAR = 2,   // weight-streaming linear layer (any epilogue; M <= 16)
+    PH_ATTN = 3,     // split-KV decode attention
+};
+
+struct PersistPhase {
+    int kind = PH_LN;
+    // PH_LINEAR: lin.M = batch; tasks = row groups of 8; nchunks = 16-byte lane
+    // chunks per row (32 bf16 or 64 int8 k each); nbt = ring batches per task and warp
+    LinearArgs lin;
+    int tasks = 0, nchunks = 0, nbt = 0;
+    // PH_LN / PH_EMBED
+    int rows = 0, h = 0;
+    float eps = 1e-5f;
+    const uint16_t *g = nullptr, *b = nullptr;
+    const float *ln_src = nullptr;      // LN: float [rows][h]
+    uint16_t *ln_dst = nullptr;         // LN: bf16 [rows][h]
+    const int *tokens = nullptr;        // EMBED: token per row
+    const uint16_t *emb = nullptr;      // EMBED: bf16 [vocab][h]
+    int vocab = 0;
+    float *emb_dst = nullptr;           // EMBED: float [rows][h]
+    const int *len = nullptr, *next_pos = nullptr;   // EMBED: pos[r][*len] = next_pos[r]
+    int *pos = nullptr;
+    int max_seq = 0;
+    // PH_ATTN: units = B * n * splits, one per thread-block visit
+    AttnDecodeArgs at;
+};
+
+struct PersistArgs {
+    const PersistPhase *phases = nullptr;
+    int nphases = 0;
+    unsigned *bar = nullptr;   // [0] barrier arrivals, [1] exit ticket, [2] abort; zero at rest
+    int *err = nullptr;
+};
+
+constexpr int kPersistMaxM = 16;    // batch rows the persistent step takes (one mma token tile)
+// Chunk geometry of a linear phase as the persistent kernel streams it.
+void persist_linear_geometry(PersistPhase &ph);
+cudaError_t persist_prepare();
+// Whether the device can hold one persistent block on every SM; the grid size.
+int persist_grid(int int8);
+cudaError_t launch_decode_persistent(const PersistArgs &pa, int int8, int grid, cudaStream_t s);
+
 }  // namespace bloom

@@ -63,8 +63,10 @@ enum {
                                  waits for the previous one to finish before it starts) */
     BLOOM_FLAG_NO_LN_FUSION = 4, /* run every LayerNorm as its own kernel instead of inside
                                     the decode linear kernel that consumes it */
-    BLOOM_FLAG_NO_TC_GEMM = 8    /* prefill linears of >= 128 tokens on the weight-streaming
+    BLOOM_FLAG_NO_TC_GEMM = 8,   /* prefill linears of >= 128 tokens on the weight-streaming
                                     kernel instead of the tensor-core (tcgen05) GEMM */
+    BLOOM_FLAG_NO_PERSISTENT = 16 /* decode steps of <= 16 sequences as one launch per
+                                    operation (CUDA graph) instead of one persistent launch */
 };
 
 typedef struct {
@@ -175,8 +177,9 @@ bloom_status bloom_destroy(bloom_model *m);
 /* Message of the last failing call on this thread ("" if none). */
 const char *bloom_last_error(void);
 
-/* Kernel launches one decode step issues (for launch accounting). */
-int32_t bloom_decode_launches(const bloom_model *m);
+/* Kernel launches one decode step of `batch` sequences issues (for launch
+ * accounting): 1 for the persistent step, else one per operation. */
+int32_t bloom_decode_launches(const bloom_model *m, int32_t batch);
 
 /* ------------------------------------------------------------------------
  * Layer-level entry points.  They run one piece of the path on caller

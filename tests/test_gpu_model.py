@@ -100,10 +100,11 @@ def test_560m_shape_generation():
     generate_parity(shape, w, steps=3, tol=2e-2)
 
 
-def test_560m_shape_random_affine_two_layers():
+@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_PERSISTENT], ids=["persistent", "per_launch"])
+def test_560m_shape_random_affine_two_layers(flags):
     shape = synth.PRESETS["560m"].with_(n_layer=2)
     w = synth.make_weights(shape, seed=1, random_affine=True)
-    generate_parity(shape, w, steps=4, tol=2e-2)
+    generate_parity(shape, w, steps=4, tol=2e-2, flags=flags)
 
 
 def test_graph_replay_equals_direct_launches():
@@ -113,7 +114,8 @@ def test_graph_replay_equals_direct_launches():
     B, T = ids.shape
     S = T + 6
     outs = []
-    for flags in (0, bg.FLAG_NO_GRAPH):
+    # the per-launch step (a CUDA graph per buffer set, or one launch per kernel)
+    for flags in (bg.FLAG_NO_PERSISTENT, bg.FLAG_NO_PERSISTENT | bg.FLAG_NO_GRAPH):
         gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S, flags=flags)
         kv = gm.new_kv(B, S)
         lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
