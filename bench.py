@@ -209,7 +209,9 @@ def run_ours(args, sh):
     w = synth.make_weights(sh, seed=0, device=dev)
     gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S,
                   flags=(bg.FLAG_NO_PDL if args.no_pdl else 0) |
-                  (bg.FLAG_NO_LN_FUSION if args.no_ln_fusion else 0))
+                  (bg.FLAG_NO_LN_FUSION if args.no_ln_fusion else 0) |
+                  (bg.FLAG_PERSISTENT if args.persistent else 0) |
+                  (bg.FLAG_NO_TC_GEMM if args.no_tc_gemm else 0))
     kv = gm.new_kv(B, S)
     ids_d, mask_d = ids.to(dev), mask.to(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
@@ -360,6 +362,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-ln-fusion", action="store_true", help="separate LayerNorm kernels")
+    ap.add_argument("--persistent", action="store_true",
+                    help="decode steps as one persistent cooperative launch (batches <= 16)")
+    ap.add_argument("--no-tc-gemm", action="store_true",
+                    help="prefill linears on the weight-streaming kernel instead of tcgen05")
     ap.add_argument("--head-traffic", type=float, default=None,
                     help="dram bytes per LM-head launch from an ncu capture of this kernel")
     args = ap.parse_args()

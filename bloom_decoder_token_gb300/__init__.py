@@ -27,7 +27,7 @@ FLAG_NO_GRAPH = 1
 FLAG_NO_PDL = 2
 FLAG_NO_LN_FUSION = 4
 FLAG_NO_TC_GEMM = 8
-FLAG_NO_PERSISTENT = 16
+FLAG_PERSISTENT = 16
 
 P = C.c_void_p
 I32 = C.c_int32

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -99,7 +100,7 @@ struct PlanEntry {
     void *out;
     void *logits;
     int B;
-    PersistPhase *phases;   // device copy
+    PersistPhase *phases;   // device copy, then the stream table (PersistStream[n])
     int n;
 };
 
@@ -132,7 +133,11 @@ struct bloom_model {
     TcMap xmaps[3];
     // persistent decode step: grid (0 = not available), barrier words, phase tables
     int pgrid = 0;
+    int pmax_phases = 0;
     unsigned *pbar = nullptr;
+    void *pscratch = nullptr;   // partial tiles + row-group tickets of the persistent step
+    float *ppart = nullptr;
+    int *pticket = nullptr;
     std::vector<PlanEntry> plans;
 };
 
@@ -185,6 +190,7 @@ extern "C" bloom_status bloom_destroy(bloom_model *m) {
     cudaSetDevice(m->dev);
     for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
     for (auto &p : m->plans) cudaFree(p.phases);
+    if (m->pscratch) cudaFree(m->pscratch);
     if (m->cap) cudaStreamDestroy(m->cap);
     if (m->ws) cudaFree(m->ws);
     delete m;
@@ -281,9 +287,24 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         linear_prepare() != cudaSuccess) {
         st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
     }
-    if (!st2 && !(cfg->flags & BLOOM_FLAG_NO_PERSISTENT)) {
+    if (!st2 && (cfg->flags & BLOOM_FLAG_PERSISTENT)) {
         m->pgrid = persist_grid(i8);   // 0: no cooperative launch of one block per SM here
+        m->pmax_phases = m->pgrid > 0 ? persist_max_phases(i8) : 0;
         cudaGetLastError();
+        if (m->pgrid > 0) {
+            int groups = (3 * h + 7) / 8;
+            groups = std::max(groups, (F + 7) / 8);
+            groups = std::max(groups, (cfg->vocab + 7) / 8);
+            const size_t pb = align256(persist_part_bytes(m->pgrid));
+            const size_t bytes = pb + (size_t)groups * 4;
+            if (cudaMalloc(&m->pscratch, bytes) != cudaSuccess ||
+                cudaMemset(m->pscratch, 0, bytes) != cudaSuccess) {
+                st2 = fail(BLOOM_E_OOM, "persistent-step scratch of %zu bytes", bytes);
+            } else {
+                m->ppart = (float *)m->pscratch;
+                m->pticket = (int *)((char *)m->pscratch + pb);
+            }
+        }
     }
     // TMA descriptors of every bf16 weight and of the activations the prefill GEMMs read
     if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_tokens >= kTcMinM) {
@@ -523,7 +544,9 @@ static cudaError_t enqueue_decode(bloom_model *m, const bloom_kv *kv, const int3
 }
 
 static bool use_persistent(const bloom_model *m, int B) {
-    return m->pgrid > 0 && B >= 1 && B <= kPersistMaxM;
+    // phases: embedding, 5 per layer (LayerNorms fused) or 7, ln_f + head
+    return m->pgrid > 0 && B >= 1 && B <= kPersistMaxM &&
+           1 + 7 * m->cfg.n_layer + 2 <= m->pmax_phases;
 }
 
 extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
@@ -586,10 +609,27 @@ static std::vector<PersistPhase> persist_plan(bloom_model *m, const bloom_kv *kv
         persist_linear_geometry(p);
         v.push_back(p);
     };
+    // a linear layer fed by LN(x): the LayerNorm runs inside the linear phase
+    // (each block normalises the rows into its staged copy) when the rows are
+    // staged in shared memory, else as a phase of its own writing `dst`
+    auto lin_ln = [&](LinearArgs a, const void *g, const void *b, uint16_t *dst) {
+        PersistPhase p;
+        p.kind = PH_LINEAR;
+        p.lin = a;
+        persist_linear_geometry(p);
+        if (p.xs) {
+            p.lin.ln_x = m->x;
+            p.lin.ln_g = (const uint16_t *)g;
+            p.lin.ln_b = (const uint16_t *)b;
+            p.lin.ln_eps = c.ln_eps;
+        } else {
+            ln(g, b, dst);
+        }
+        v.push_back(p);
+    };
     const int splits = persist_splits(m, B, kv->max_seq);
     for (int l = 0; l < c.n_layer; ++l) {
         const bloom_layer_weights &L = m->layers[l];
-        ln(L.ln1_g, L.ln1_b, m->a);
         LinearArgs q = lin_args(L.qkv, i8, m->a, B, 3 * h, h, EPI_QKV);
         q.q_out = m->q;
         q.k_cache = kp.k + kp.layer_elems * l;
@@ -599,7 +639,7 @@ static std::vector<PersistPhase> persist_plan(bloom_model *m, const bloom_kv *kv
         q.head_dim = d;
         q.max_seq = kv->max_seq;
         q.err = m->err;
-        lin(q);
+        lin_ln(q, L.ln1_g, L.ln1_b, m->a);
         PersistPhase at;
         at.kind = PH_ATTN;
         at.at.q = m->q;
@@ -621,15 +661,13 @@ static std::vector<PersistPhase> persist_plan(bloom_model *m, const bloom_kv *kv
         LinearArgs od = lin_args(L.o, i8, m->o, B, h, h, EPI_RESID32);
         od.out32 = m->x;
         lin(od);
-        ln(L.ln2_g, L.ln2_b, m->a);
         LinearArgs up = lin_args(L.up, i8, m->a, B, F, h, EPI_GELU);
         up.out = m->u;
-        lin(up);
+        lin_ln(up, L.ln2_g, L.ln2_b, m->a);
         LinearArgs dn = lin_args(L.down, i8, m->u, B, h, F, EPI_RESID32);
         dn.out32 = m->x;
         lin(dn);
     }
-    ln(m->lnf_g, m->lnf_b, m->xl);
     LinearArgs hd;
     hd.w = m->word_emb;
     hd.x = m->xl;
@@ -643,7 +681,7 @@ static std::vector<PersistPhase> persist_plan(bloom_model *m, const bloom_kv *kv
     hd.out_tokens = out;
     hd.len_inc = kp.len;
     hd.next_pos = kp.next_pos;
-    lin(hd);
+    lin_ln(hd, m->lnf_g, m->lnf_b, m->xl);
     return v;
 }
 
@@ -658,10 +696,22 @@ static bloom_status decode_persistent(bloom_model *m, const bloom_kv *kv, const 
         }
     if (!pe) {
         const std::vector<PersistPhase> v = persist_plan(m, kv, next, out, logits);
+        std::vector<PersistStream> st(v.size());
+        for (size_t i = 0; i < v.size(); ++i) {
+            if (v[i].kind != PH_LINEAR) continue;
+            st[i].w = (const char *)v[i].lin.w;
+            st[i].tb = v[i].tb;
+            st[i].nbt = v[i].nbt;
+            st[i].N = v[i].lin.N;
+            st[i].row_bytes = v[i].lin.K * (v[i].lin.int8 ? 1 : 2);
+        }
+        const size_t pb = v.size() * sizeof(PersistPhase), sb = st.size() * sizeof(PersistStream);
+        std::vector<char> blob(pb + sb);
+        memcpy(blob.data(), v.data(), pb);
+        memcpy(blob.data() + pb, st.data(), sb);
         PersistPhase *d = nullptr;
-        CK(cudaMalloc(&d, v.size() * sizeof(PersistPhase)));
-        cudaError_t e = cudaMemcpyAsync(d, v.data(), v.size() * sizeof(PersistPhase),
-                                        cudaMemcpyHostToDevice, s);
+        CK(cudaMalloc(&d, blob.size()));
+        cudaError_t e = cudaMemcpyAsync(d, blob.data(), blob.size(), cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // v is freed on return
         if (e != cudaSuccess) {
             cudaFree(d);
@@ -676,9 +726,12 @@ static bloom_status decode_persistent(bloom_model *m, const bloom_kv *kv, const 
     }
     PersistArgs pa;
     pa.phases = pe->phases;
+    pa.streams = reinterpret_cast<const PersistStream *>(pe->phases + pe->n);
     pa.nphases = pe->n;
     pa.bar = m->pbar;
     pa.err = m->err;
+    pa.part = m->ppart;
+    pa.rg_ticket = m->pticket;
     CK(launch_decode_persistent(pa, m->cfg.weight_dtype == BLOOM_WEIGHT_INT8, m->pgrid, s));
     return BLOOM_OK;
 }

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     extern __shared__ __align__(16) unsigned char xs[];   // LNF: [M][K*2 + 64] bf16
     __shared__ float red[kLinWarps][MT][4][kWarp];
     __shared__ unsigned long long s_best[EPI == EPI_ARGMAX ? kMaxBatch : 1];
-    __shared__ float s_sum[2 * kLinWarps];
+    __shared__ float s_sum[3 * kLinWarps];
     __shared__ int s_last;
 
     griddep_launch();

@@ -178,12 +178,15 @@ enum PhaseKind : int {
     PH_ATTN = 3,     // split-KV decode attention
 };
 
-struct PersistPhase {
+struct alignas(16) PersistPhase {
     int kind = PH_LN;
-    // PH_LINEAR: lin.M = batch; tasks = row groups of 8; nchunks = 16-byte lane
-    // chunks per row (32 bf16 or 64 int8 k each); nbt = ring batches per task and warp
+    // PH_LINEAR: lin.M = batch; tasks = row groups of 8; nchunks = 64-byte chunks
+    // per row (32 bf16 or 64 int8 k each); nbt = 4-chunk batches per row group;
+    // tb = tasks * nbt, the phase's batches, split into one piece per warp
     LinearArgs lin;
     int tasks = 0, nchunks = 0, nbt = 0;
+    long long tb = 0;
+    int xs = 0;                         // activations staged in shared memory for the phase
     // PH_LN / PH_EMBED
     int rows = 0, h = 0;
     float eps = 1e-5f;
@@ -201,11 +204,21 @@ struct PersistPhase {
     AttnDecodeArgs at;
 };
 
+// A phase's weight stream as the persistent kernel walks it (tb = 0: no weights).
+struct PersistStream {
+    const char *w = nullptr;
+    long long tb = 0;
+    int nbt = 0, N = 0, row_bytes = 0, pad = 0;
+};
+
 struct PersistArgs {
     const PersistPhase *phases = nullptr;
+    const PersistStream *streams = nullptr;   // one per phase
     int nphases = 0;
     unsigned *bar = nullptr;   // [0] barrier arrivals, [1] exit ticket, [2] abort; zero at rest
     int *err = nullptr;
+    float *part = nullptr;     // [grid * 8 warps][2][128] partial tiles of shared row groups
+    int *rg_ticket = nullptr;  // [largest row-group count of any phase], zero at rest
 };
 
 constexpr int kPersistMaxM = 16;    // batch rows the persistent step takes (one mma token tile)
@@ -214,6 +227,9 @@ void persist_linear_geometry(PersistPhase &ph);
 cudaError_t persist_prepare();
 // Whether the device can hold one persistent block on every SM; the grid size.
 int persist_grid(int int8);
+size_t persist_part_bytes(int grid);
+int persist_max_phases(int int8);       // phases whose stream table fits in shared memory
+size_t persist_smem_bytes(int nphases);
 cudaError_t launch_decode_persistent(const PersistArgs &pa, int int8, int grid, cudaStream_t s);
 
 }  // namespace bloom

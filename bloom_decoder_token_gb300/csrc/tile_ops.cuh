@@ -84,53 +84,93 @@ __device__ __forceinline__ void tile_epilogue(const LinearArgs &a, const float (
     }
 }
 
+// Merge of two (count, mean, sum of squared deviations) summaries of a set of
+// values (the pairwise update of Chan, Golub and LeVeque).
+__device__ __forceinline__ void stats_merge(float &n, float &mean, float &m2, float nb, float meanb,
+                                            float m2b) {
+    const float nn = n + nb;
+    if (nb == 0.f) return;
+    if (n == 0.f) {
+        n = nb;
+        mean = meanb;
+        m2 = m2b;
+        return;
+    }
+    const float delta = meanb - mean;
+    const float f = nb / nn;
+    mean += delta * f;
+    m2 += m2b + delta * delta * n * f;
+    n = nn;
+}
+
 // LayerNorm of the M float32 rows a.ln_x[M][K] into shared memory as bf16
 // (row pitch px bytes); float32 statistics, biased variance, eps inside the
 // square root.  Rows are spread over the CTA's warps (a team of 256 / rows
-// threads per row, at least one warp); the statistics come from one pass of
-// sums shifted by the row's first element (sum (x-s), sum (x-s)^2), which keeps
-// the variance free of cancellation when |mean| >> std.  All threads of the CTA
-// call it (two barriers).
+// threads per row, at least one warp).  Every load of a row is issued before
+// any is used (one L2 round trip), each thread summarises its values as
+// (count, mean, squared deviations) around its own first value and the
+// summaries are merged pairwise (no E[x^2] - mean^2 cancellation); the gamma /
+// beta lines are pulled into L1 meanwhile, so that the normalising pass, which
+// re-reads the row from L1, waits on nothing.  All threads of the CTA call it.
 __device__ __forceinline__ void layernorm_rows_to_smem(const LinearArgs &a, unsigned char *xs,
                                                        int px, float *s_sum, int tid, int warp,
                                                        int lane) {
+    constexpr int UL = 8;                   // float4 loads in flight per thread
     const int nthr = blockDim.x, nw = nthr / 32;
     int team_w = nw;                        // warps per row
     while (team_w > 1 && team_w > nw / (a.M < nw ? a.M : nw)) team_w >>= 1;
     const int teams = nw / team_w;
     const int team = warp / team_w, tw = warp % team_w;
     const int tthr = team_w * 32, ttid = tw * 32 + lane;
-    float *stat = s_sum;                    // [nw][2]
+    float *stat = s_sum;                    // [nw][3] (s_sum holds 3 * nw floats)
     for (int m0 = 0; m0 < a.M; m0 += teams) {
         const int m = m0 + team;
-        float s1 = 0.f, s2 = 0.f, shift = 0.f;
+        float n = 0.f, mean = 0.f, m2 = 0.f;
         if (m < a.M) {
             const float *xr = a.ln_x + (size_t)m * a.K;
-            shift = xr[0];
-            for (int k = ttid * 4; k < a.K; k += 4 * tthr) {
-                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
-                const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
-                s1 += (d0 + d1) + (d2 + d3);
-                s2 += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+            for (int kb = ttid * 4; kb < a.K; kb += 4 * tthr * UL) {
+                float4 v[UL];
+#pragma unroll
+                for (int u = 0; u < UL; ++u) {
+                    const int k = kb + u * 4 * tthr;
+                    if (k < a.K) {
+                        v[u] = *reinterpret_cast<const float4 *>(xr + k);
+                        // the normalising pass needs gamma / beta of these k from L1
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.ln_g + k));
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.ln_b + k));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < UL; ++u) {
+                    const int k = kb + u * 4 * tthr;
+                    if (k < a.K) {
+                        // summary of these four values, merged into the running one
+                        const float c = 0.25f * ((v[u].x + v[u].y) + (v[u].z + v[u].w));
+                        const float d0 = v[u].x - c, d1 = v[u].y - c, d2 = v[u].z - c, d3 = v[u].w - c;
+                        stats_merge(n, mean, m2, 4.f, c, (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3));
+                    }
+                }
             }
         }
-        s1 = warp_sum(s1);
-        s2 = warp_sum(s2);
+        // merge over the warp, then over the team's warps
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+            const float mb = __shfl_xor_sync(0xffffffffu, mean, o);
+            const float qb = __shfl_xor_sync(0xffffffffu, m2, o);
+            stats_merge(n, mean, m2, nb, mb, qb);
+        }
         if (lane == 0) {
-            stat[2 * warp] = s1;
-            stat[2 * warp + 1] = s2;
+            stat[3 * warp] = n;
+            stat[3 * warp + 1] = mean;
+            stat[3 * warp + 2] = m2;
         }
         __syncthreads();
         if (m < a.M) {
-            float t1 = 0.f, t2 = 0.f;
-            for (int w = team * team_w; w < (team + 1) * team_w; ++w) {
-                t1 += stat[2 * w];
-                t2 += stat[2 * w + 1];
-            }
-            const float inv_k = 1.f / (float)a.K;
-            const float dm = t1 * inv_k;
-            const float var = fmaxf(t2 * inv_k - dm * dm, 0.f);
-            const float mean = shift + dm;
+            float tn = 0.f, tmean = 0.f, tm2 = 0.f;
+            for (int w = team * team_w; w < (team + 1) * team_w; ++w)
+                stats_merge(tn, tmean, tm2, stat[3 * w], stat[3 * w + 1], stat[3 * w + 2]);
+            const float var = fmaxf(tm2 / (float)a.K, 0.f);
             const float rstd = rsqrtf(var + a.ln_eps);
             const float *xr = a.ln_x + (size_t)m * a.K;
             uint16_t *dst = reinterpret_cast<uint16_t *>(xs + (size_t)m * px);
@@ -139,10 +179,10 @@ __device__ __forceinline__ void layernorm_rows_to_smem(const LinearArgs &a, unsi
                 const uint2 gg = *reinterpret_cast<const uint2 *>(a.ln_g + k);
                 const uint2 bb = *reinterpret_cast<const uint2 *>(a.ln_b + k);
                 uint2 o;
-                o.x = pack_bf2((v.x - mean) * rstd * bf_lo(gg.x) + bf_lo(bb.x),
-                               (v.y - mean) * rstd * bf_hi(gg.x) + bf_hi(bb.x));
-                o.y = pack_bf2((v.z - mean) * rstd * bf_lo(gg.y) + bf_lo(bb.y),
-                               (v.w - mean) * rstd * bf_hi(gg.y) + bf_hi(bb.y));
+                o.x = pack_bf2((v.x - tmean) * rstd * bf_lo(gg.x) + bf_lo(bb.x),
+                               (v.y - tmean) * rstd * bf_hi(gg.x) + bf_hi(bb.x));
+                o.y = pack_bf2((v.z - tmean) * rstd * bf_lo(gg.y) + bf_lo(bb.y),
+                               (v.w - tmean) * rstd * bf_hi(gg.y) + bf_hi(bb.y));
                 *reinterpret_cast<uint2 *>(dst + k) = o;
             }
         }

@@ -65,8 +65,10 @@ enum {
                                     the decode linear kernel that consumes it */
     BLOOM_FLAG_NO_TC_GEMM = 8,   /* prefill linears of >= 128 tokens on the weight-streaming
                                     kernel instead of the tensor-core (tcgen05) GEMM */
-    BLOOM_FLAG_NO_PERSISTENT = 16 /* decode steps of <= 16 sequences as one launch per
-                                    operation (CUDA graph) instead of one persistent launch */
+    BLOOM_FLAG_PERSISTENT = 16   /* decode steps of <= 16 sequences as one persistent
+                                    cooperative launch (all layers as phases separated by grid
+                                    barriers) instead of one launch per operation replayed as a
+                                    CUDA graph */
 };
 
 typedef struct {

@@ -100,7 +100,7 @@ def test_560m_shape_generation():
     generate_parity(shape, w, steps=3, tol=2e-2)
 
 
-@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_PERSISTENT], ids=["persistent", "per_launch"])
+@pytest.mark.parametrize("flags", [0, bg.FLAG_PERSISTENT], ids=["per_launch", "persistent"])
 def test_560m_shape_random_affine_two_layers(flags):
     shape = synth.PRESETS["560m"].with_(n_layer=2)
     w = synth.make_weights(shape, seed=1, random_affine=True)
@@ -115,7 +115,7 @@ def test_graph_replay_equals_direct_launches():
     S = T + 6
     outs = []
     # the per-launch step (a CUDA graph per buffer set, or one launch per kernel)
-    for flags in (bg.FLAG_NO_PERSISTENT, bg.FLAG_NO_PERSISTENT | bg.FLAG_NO_GRAPH):
+    for flags in (0, bg.FLAG_NO_GRAPH):
         gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S, flags=flags)
         kv = gm.new_kv(B, S)
         lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)

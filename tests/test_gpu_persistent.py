@@ -35,7 +35,7 @@ def built():
 def test_persistent_matches_oracle(name, over, seed, affine, tol):
     shape = synth.PRESETS[name].with_(**over)
     w = synth.make_weights(shape, seed=seed, random_affine=affine)
-    generate_parity(shape, w, steps=5, tol=tol)
+    generate_parity(shape, w, steps=5, tol=tol, flags=bg.FLAG_PERSISTENT)
 
 
 def run_steps(w, shape, flags, steps=6):
@@ -59,10 +59,10 @@ def run_steps(w, shape, flags, steps=6):
 def test_persistent_is_deterministic_and_matches_per_launch_step():
     shape = synth.PRESETS["560m"].with_(n_layer=3, vocab=5000, batch=8)
     w = synth.make_weights(shape, seed=8, random_affine=True).to(DEV)
-    t1, l1 = run_steps(w, shape, 0)
-    t2, l2 = run_steps(w, shape, 0)
+    t1, l1 = run_steps(w, shape, bg.FLAG_PERSISTENT)
+    t2, l2 = run_steps(w, shape, bg.FLAG_PERSISTENT)
     assert torch.equal(t1, t2) and torch.equal(l1, l2)
-    t3, l3 = run_steps(w, shape, bg.FLAG_NO_PERSISTENT)
+    t3, l3 = run_steps(w, shape, 0)
     # same arithmetic up to the LayerNorm statistics' summation order
     assert torch.equal(t1[0], t3[0])   # the prefill is the same kernels
     assert max_abs(l1[0], l3[0].double().numpy()) <= 2e-2
@@ -71,12 +71,13 @@ def test_persistent_is_deterministic_and_matches_per_launch_step():
 def test_launch_accounting_and_fallback_above_16():
     shape = synth.PRESETS["block"].with_(vocab=700, batch=17, ragged=True)
     w = synth.make_weights(shape, seed=9, random_affine=True)
-    gm = bg.Model(w.to(DEV), max_batch=17, max_tokens=17 * shape.prompt, max_seq=shape.max_seq)
+    gm = bg.Model(w.to(DEV), max_batch=17, max_tokens=17 * shape.prompt, max_seq=shape.max_seq,
+                  flags=bg.FLAG_PERSISTENT)
     assert gm.decode_launches(8) == 1
     assert gm.decode_launches(17) > 1
     gm.close()
-    gmp = bg.Model(w.to(DEV), max_batch=17, max_tokens=17 * shape.prompt, max_seq=shape.max_seq,
-                   flags=bg.FLAG_NO_PERSISTENT)
+    gmp = bg.Model(w.to(DEV), max_batch=17, max_tokens=17 * shape.prompt, max_seq=shape.max_seq)
     assert gmp.decode_launches(8) > 1
     gmp.close()
-    generate_parity(shape, w, steps=3, tol=2e-2)   # 17 sequences: per-launch step
+    # 17 sequences: the per-launch step even when the persistent one is asked for
+    generate_parity(shape, w, steps=3, tol=2e-2, flags=bg.FLAG_PERSISTENT)
