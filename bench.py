@@ -12,6 +12,7 @@ Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 on its own GPU (sequences are independent; no collective on the data path).
 """
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -61,6 +62,69 @@ def decode_step_bytes(sh: synth.Shape, B: int, keys: int) -> int:
 
 def head_launch_bytes(sh: synth.Shape, B: int) -> int:
     return sh.vocab * sh.hidden * 2 + B * sh.hidden * 2 + B * 4
+
+
+# ------------------------------------------------------------------ measured DRAM traffic
+HEAD_SOURCES = ["k_linear.cu", "tile_ops.cuh", "common.cuh", "kernels.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lm_head_traffic.json")
+
+
+def head_source_digest() -> str:
+    h = hashlib.sha256()
+    for f in HEAD_SOURCES:
+        with open(os.path.join(ROOT, "bloom_decoder_token_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def head_traffic(sh: synth.Shape, B: int):
+    """dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch as an
+    ncu capture recorded it for this workload, or None when there is no capture
+    for it or the kernel's sources changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE))
+    if d.get("kernel_source_sha256") != head_source_digest():
+        return None
+    return d.get("bytes_per_launch", {}).get(f"{sh.name}/B{B}")
+
+
+def measure_head(gm, sh, B, dev, stream, reps=50):
+    """Dominant kernel: the tied LM head + argmax (largest single weight stream),
+    timed alone with CUDA events on its stream."""
+    xn = torch.randn(B, sh.hidden, device=dev).to(torch.bfloat16)
+    ht = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        gm.lm_head(xn, ht)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        gm.lm_head(xn, ht)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    head_ms = a.elapsed_time(b) / reps
+    head_bytes = head_launch_bytes(sh, B)
+    return head_ms, head_bytes, head_bytes / (head_ms / 1e3) / 1e9
+
+
+def run_roofline_only(args, sh):
+    """Only the dominant kernel's measurement (the command an ncu capture of its
+    DRAM counters runs)."""
+    import bloom_decoder_token_gb300 as bg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    B = sh.batch
+    w = synth.make_weights(sh.with_(n_layer=1), seed=0, device=dev)
+    gm = bg.Model(w, max_batch=B, max_tokens=B * sh.prompt, max_seq=sh.max_seq)
+    head_ms, head_bytes, head_gbs = measure_head(gm, sh, B, dev, torch.cuda.current_stream(dev))
+    hbm, src = peaks()
+    print(json.dumps({"roofline_only": True, "workload": f"{sh.name}/B{B}", "launch_ms": head_ms,
+                      "bytes_per_launch": head_bytes, "achieved_gbs": head_gbs,
+                      "frac": head_gbs / hbm, "peak_source": src,
+                      "kernel_source_sha256": head_source_digest()}), flush=True)
+    gm.close()
 
 
 # ------------------------------------------------------------------ clocks
@@ -263,24 +327,8 @@ def run_ours(args, sh):
     hbm, src = peaks()
     dec_gbs = step_bytes / (dec_ms / 1e3) / 1e9
 
-    # dominant kernel: the tied LM head + argmax (largest single weight stream)
-    xn = torch.randn(B, sh.hidden, device=dev).to(torch.bfloat16)
-    ht = torch.empty(B, dtype=torch.int32, device=dev)
-    for _ in range(3):
-        gm.lm_head(xn, ht)
-    torch.cuda.synchronize(dev)
-    reps = 50
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        gm.lm_head(xn, ht)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    head_ms = a.elapsed_time(b) / reps
-    head_bytes = head_launch_bytes(sh, B)
-    head_gbs = head_bytes / (head_ms / 1e3) / 1e9
-    traffic = args.head_traffic
+    head_ms, head_bytes, head_gbs = measure_head(gm, sh, B, dev, stream)
+    traffic = args.head_traffic if args.head_traffic is not None else head_traffic(sh, B)
 
     # end to end through the public API with host buffers
     ids_h = ids.contiguous().pin_memory()
@@ -357,6 +405,7 @@ def main():
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--new-tokens", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None, help="decoder layers (default: the preset's)")
+    ap.add_argument("--prompt", type=int, default=None, help="padded prompt length (default: the preset's)")
     ap.add_argument("--cpu-decode-steps", type=int, default=8)
     ap.add_argument("--ref-decode-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -367,7 +416,10 @@ def main():
     ap.add_argument("--no-tc-gemm", action="store_true",
                     help="prefill linears on the weight-streaming kernel instead of tcgen05")
     ap.add_argument("--head-traffic", type=float, default=None,
-                    help="dram bytes per LM-head launch from an ncu capture of this kernel")
+                    help="dram bytes per LM-head launch from an ncu capture of this kernel "
+                         "(default: the recorded capture, if the kernel is unchanged)")
+    ap.add_argument("--roofline-only", action="store_true",
+                    help="only time the dominant kernel (LM head + argmax) and print its line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -378,8 +430,12 @@ def main():
         sh = sh.with_(new_tokens=args.new_tokens)
     if args.layers:
         sh = sh.with_(n_layer=args.layers)
+    if args.prompt:
+        sh = sh.with_(prompt=args.prompt)
     if args.impl == "reference":
         run_reference(args, sh)
+    elif args.roofline_only:
+        run_roofline_only(args, sh)
     else:
         run_ours(args, sh)
 

@@ -48,10 +48,19 @@ def max_abs(a, b) -> float:
 
 
 def assert_stream_close(gpu, ref, tol=2e-2, what=""):
-    """Residual-stream gate: |gpu - ref| <= tol * max(1, |ref|)."""
+    """Residual-stream gate: |gpu - ref| <= tol * max(1, |ref|, rms of ref's row).
+
+    The path rounds the LayerNorm outputs, q / k / v, the attention output and
+    the MLP intermediate to bf16 (relative error up to 2^-9 each); a block's
+    contribution to the residual is a sum over K of such rounded values times
+    weights, so its error grows with the row's scale, not with each element's
+    own magnitude.  A restatement that rounds at the same points deviates from
+    the float64 oracle by as much (7b1-width block, rms 2.7: max 4.2e-2), so
+    elements small within a large row are bounded by the row's rms."""
     g, r = f64(gpu), f64(ref)
     err = np.abs(g - r)
-    bound = tol * np.maximum(1.0, np.abs(r))
+    rms = np.sqrt(np.mean(r * r, axis=-1, keepdims=True)) if r.ndim else np.abs(r)
+    bound = tol * np.maximum(np.maximum(1.0, np.abs(r)), rms)
     if (err > bound).any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{what}: max|err| {err.max():.3e}; worst at {i}: gpu {g[i]} ref {r[i]}")
