@@ -91,7 +91,8 @@ struct TcMap {
     alignas(64) unsigned char b[128];
 };
 enum { TC_QKV = 0, TC_O = 1, TC_UP = 2, TC_DOWN = 3, TC_PER_LAYER = 4 };
-enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2 };
+enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2, TC_X_XL = 3 };
+constexpr int kTcNtClasses = 5;   // decode token columns 16, 32, 64, 128, 256
 
 // Phase table of the persistent decode step for one set of step buffers.
 struct PlanEntry {
@@ -131,6 +132,14 @@ struct bloom_model {
     bool tc = false;
     std::vector<TcMap> wmaps;
     TcMap xmaps[3];
+    // tensor-core decode linear: weight maps (box 128 rows) [layer][TC_*] then the
+    // head; activation maps [TC_X_*][token-column class]; split-K scratch
+    bool tcd = false;
+    std::vector<TcMap> dwmaps;
+    TcMap dxmaps[4][kTcNtClasses];
+    void *gv_scratch = nullptr;
+    float *gv_part = nullptr;
+    int *gv_ticket = nullptr;
     // persistent decode step: grid (0 = not available), barrier words, phase tables
     int pgrid = 0;
     int pmax_phases = 0;
@@ -191,6 +200,7 @@ extern "C" bloom_status bloom_destroy(bloom_model *m) {
     for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
     for (auto &p : m->plans) cudaFree(p.phases);
     if (m->pscratch) cudaFree(m->pscratch);
+    if (m->gv_scratch) cudaFree(m->gv_scratch);
     if (m->cap) cudaStreamDestroy(m->cap);
     if (m->ws) cudaFree(m->ws);
     delete m;
@@ -286,6 +296,47 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking) != cudaSuccess ||
         linear_prepare() != cudaSuccess) {
         st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    // decode linears of >= kTcDecodeMinM tokens on the tensor cores
+    if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_batch >= kTcDecodeMinM) {
+        bool ok = gemm_map_bytes() == sizeof(TcMap);
+        const int bw = gemv_tc_box_rows_w();
+        m->dwmaps.resize((size_t)cfg->n_layer * TC_PER_LAYER + 1);
+        for (int l = 0; ok && l < cfg->n_layer; ++l) {
+            const bloom_layer_weights &L = w->layers[l];
+            TcMap *wm = &m->dwmaps[(size_t)l * TC_PER_LAYER];
+            ok = gemm_make_map(wm[TC_QKV].b, L.qkv.w, 3 * h, h, bw) &&
+                 gemm_make_map(wm[TC_O].b, L.o.w, h, h, bw) &&
+                 gemm_make_map(wm[TC_UP].b, L.up.w, F, h, bw) &&
+                 gemm_make_map(wm[TC_DOWN].b, L.down.w, h, F, bw);
+        }
+        ok = ok && gemm_make_map(m->dwmaps.back().b, w->word_emb, cfg->vocab, h, bw);
+        const int ntmax = gemv_tc_nt(cfg->max_batch);
+        for (int ci = 0; ok && ci < kTcNtClasses && (16 << ci) <= ntmax; ++ci) {
+            const int nt = 16 << ci;
+            ok = gemm_make_map(m->dxmaps[TC_X_A][ci].b, m->a, cfg->max_batch, h, nt) &&
+                 gemm_make_map(m->dxmaps[TC_X_O][ci].b, m->o, cfg->max_batch, h, nt) &&
+                 gemm_make_map(m->dxmaps[TC_X_U][ci].b, m->u, cfg->max_batch, F, nt) &&
+                 gemm_make_map(m->dxmaps[TC_X_XL][ci].b, m->xl, cfg->max_batch, h, nt);
+        }
+        size_t part = 0;
+        const int shapes[4][2] = {{3 * h, h}, {h, h}, {F, h}, {h, F}};
+        for (auto &nk : shapes)
+            part = std::max(part, gemv_tc_part_floats(nk[0], nk[1], cfg->max_batch, m->num_sms));
+        const size_t tickets = (size_t)(std::max(3 * h, F) + 127) / 128;
+        const size_t pb = align256(part * 4), bytes = pb + tickets * 4;
+        if (!ok) {
+            st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the decode linears could not be encoded");
+        } else if (gemv_tc_prepare() != cudaSuccess) {
+            st2 = fail(BLOOM_E_CUDA, "decode linear setup: %s", cudaGetErrorString(cudaGetLastError()));
+        } else if (cudaMalloc(&m->gv_scratch, bytes) != cudaSuccess ||
+                   cudaMemset(m->gv_scratch, 0, bytes) != cudaSuccess) {
+            st2 = fail(BLOOM_E_OOM, "decode linear scratch of %zu bytes", bytes);
+        } else {
+            m->gv_part = (float *)m->gv_scratch;
+            m->gv_ticket = (int *)((char *)m->gv_scratch + pb);
+            m->tcd = true;
+        }
     }
     if (!st2 && (cfg->flags & BLOOM_FLAG_PERSISTENT)) {
         m->pgrid = persist_grid(i8);   // 0: no cooperative launch of one block per SM here
@@ -405,10 +456,33 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
 
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
 // kTcMinM tokens or more, else the weight-streaming kernel.
+// Decode linear on the tensor cores; wmap_index into dwmaps, xmap one of TC_X_*.
+static cudaError_t run_gemv_tc(bloom_model *m, const LinearArgs &a, size_t wmap_index, int xmap,
+                               cudaStream_t s) {
+    const int nt = gemv_tc_nt(a.M);
+    int ci = 0;
+    while ((16 << ci) < nt) ++ci;
+    GemvTcArgs g;
+    g.a = a;
+    g.splits = gemv_tc_splits(a.N, a.K, m->num_sms, a.epi);
+    g.part = m->gv_part;
+    g.ticket = m->gv_ticket;
+    return launch_gemv_tc(m->dwmaps[wmap_index].b, m->dxmaps[xmap][ci].b, g, nt, s);
+}
+
+static bool use_gemv_tc(const bloom_model *m, const LinearArgs &a) {
+    return m->tcd && a.T == 0 && a.M >= kTcDecodeMinM && a.M <= m->cfg.max_batch && !a.ln_x &&
+           !a.int8;
+}
+
+// A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
+// kTcMinM tokens or more, the tensor-core decode linear for kTcDecodeMinM
+// tokens or more, else the weight-streaming kernel.
 static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wmap, int xmap,
                               cudaStream_t s) {
     if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x)
         return launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
+    if (use_gemv_tc(m, a)) return run_gemv_tc(m, a, (size_t)l * TC_PER_LAYER + wmap, xmap, s);
     return launch_linear(a, m->num_sms, s);
 }
 
@@ -524,6 +598,7 @@ static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int strid
                                          B, c.hidden, c.ln_eps, m->xl, stride, last, s))) {
         return e;
     }
+    if (use_gemv_tc(m, a)) return run_gemv_tc(m, a, m->dwmaps.size() - 1, TC_X_XL, s);
     return launch_linear(a, m->num_sms, s);
 }
 
@@ -551,7 +626,20 @@ static bool use_persistent(const bloom_model *m, int B) {
 
 extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
     if (!m) return 0;
-    return use_persistent(m, batch) ? 1 : 1 + 7 * m->cfg.n_layer + 2;
+    if (use_persistent(m, batch)) return 1;
+    // embedding; per layer LN1, QKV, attention, dense, LN2, up, down; ln_f, head --
+    // less the LayerNorm launches that the linear kernels absorb
+    const bool fusable = !(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION);
+    LinearArgs t;
+    t.M = batch;
+    t.K = m->cfg.hidden;
+    t.int8 = m->cfg.weight_dtype == BLOOM_WEIGHT_INT8;
+    t.epi = EPI_QKV;
+    const int block_ln = (fusable && linear_can_fuse_ln(t)) ? 0 : 2;
+    t.int8 = 0;
+    t.epi = EPI_ARGMAX;
+    const int head_ln = (fusable && linear_can_fuse_ln(t)) ? 0 : 1;
+    return 1 + (5 + block_ln) * m->cfg.n_layer + 1 + head_ln;
 }
 
 // Key ranges per (sequence, head) in the persistent step: one visit of every
@@ -1006,6 +1094,47 @@ extern "C" bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, in
     LinearArgs a = lin_args(*lin, 0, (const uint16_t *)x, M, N, K, epilogue);
     a.out = (uint16_t *)y;
     CK(launch_gemm_tc(mx.b, mw.b, a, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_op_linear_tc(const bloom_linear *lin, const void *x, int32_t M,
+                                           int32_t N, int32_t K, int32_t epilogue, void *y,
+                                           void *stream) {
+    g_pdl = true;
+    if (!lin) return fail(BLOOM_E_INVALID, "null argument");
+    bloom_status st = check_linear(*lin, 0, N, K, "op", -1);
+    if (st) return st;
+    if (M < 0 || N < 1) return fail(BLOOM_E_INVALID, "M=%d N=%d", M, N);
+    if (M > kMaxBatch) return fail(BLOOM_E_CAPACITY, "M=%d above %d", M, kMaxBatch);
+    if (epilogue < BLOOM_EPI_STORE || epilogue > BLOOM_EPI_RESID)
+        return fail(BLOOM_E_INVALID, "epilogue %d", epilogue);
+    if (M == 0) return BLOOM_OK;
+    if (!x || !y) return fail(BLOOM_E_INVALID, "null argument");
+    if (!aligned16(x)) return fail(BLOOM_E_INVALID, "x not 16-byte aligned");
+    const int sms = device_sms();
+    const int nt = gemv_tc_nt(M);
+    TcMap mx, mw;
+    if (gemm_map_bytes() != sizeof(TcMap) || !gemm_make_map(mx.b, x, M, K, nt) ||
+        !gemm_make_map(mw.b, lin->w, N, K, gemv_tc_box_rows_w()))
+        return fail(BLOOM_E_UNSUPPORTED, "TMA descriptors could not be encoded");
+    CK(gemv_tc_prepare());
+    cudaStream_t s = (cudaStream_t)stream;
+    GemvTcArgs g;
+    g.a = lin_args(*lin, 0, (const uint16_t *)x, M, N, K, epilogue);
+    g.a.out = (uint16_t *)y;
+    g.splits = gemv_tc_splits(N, K, sms, epilogue);
+    void *scratch = nullptr;
+    if (g.splits > 1) {
+        const size_t pb = align256(gemv_tc_part_floats(N, K, M, sms) * 4);
+        const size_t bytes = pb + (size_t)((N + 127) / 128) * 4;
+        CK(cudaMallocAsync(&scratch, bytes, s));
+        CK(cudaMemsetAsync((char *)scratch + pb, 0, bytes - pb, s));
+        g.part = (float *)scratch;
+        g.ticket = (int *)((char *)scratch + pb);
+    }
+    cudaError_t e = launch_gemv_tc(mw.b, mx.b, g, nt, s);
+    if (scratch) cudaFreeAsync(scratch, s);
+    CK(e);
     return BLOOM_OK;
 }
 

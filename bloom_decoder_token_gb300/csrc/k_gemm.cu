@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ops.cuh"
 
 namespace bloom {
 
@@ -38,93 +39,6 @@ constexpr int kTcABytes = kTcBM * kTcBK * 2;     // 16 KB
 constexpr int kTcBBytes = kTcBN * kTcBK * 2;     // 32 KB
 constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
 constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 1024;   // + 1 KB alignment slack
-constexpr long long kTcWaitCycles = 4000000000ll;
-
-__device__ __forceinline__ uint32_t tc_smem(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void tc_mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem(bar)), "r"(count));
-}
-__device__ __forceinline__ bool tc_mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(tc_smem(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool tc_mbar_wait(uint64_t *bar, uint32_t parity,
-                                             long long limit = kTcWaitCycles) {
-    if (tc_mbar_test(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (tc_mbar_test(bar, parity)) return true;
-        if ((i & 15u) == 0 && clock64() - t0 > limit) return false;
-    }
-}
-__device__ __forceinline__ void tc_tma_2d(void *dst, const CUtensorMap *map, int c0, int c1,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(tc_smem(dst)),
-        "l"(map), "r"(c0), "r"(c1), "r"(tc_smem(bar))
-        : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 bytes, 8-row atoms of 1024 bytes (stride 1024),
-// descriptor version 1, swizzle mode 2 (128B).
-__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3fffu);            // start address
-    d |= (uint64_t)1 << 16;                              // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;                    // stride byte offset
-    d |= (uint64_t)1 << 46;                              // version
-    d |= (uint64_t)2 << 61;                              // 128-byte swizzle
-    return d;
-}
-
-// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            tc_smem(bar))
-        : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Epilogue of 32 consecutive features [nb, nb + 32) of token row m (v = the
 // accumulators); features >= a.N are dropped.
 template <int EPI>

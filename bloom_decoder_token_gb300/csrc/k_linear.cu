@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
         }
         griddep_wait();
         waited = true;
-        layernorm_rows_to_smem(a, xs, PX, s_sum, threadIdx.x, warp, lane);
+        layernorm_rows_to_smem_shifted(a, xs, PX, s_sum, threadIdx.x, warp, lane);
     }
 
     for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {

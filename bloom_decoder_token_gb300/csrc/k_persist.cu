@@ -427,7 +427,7 @@ __device__ __noinline__ void linear_phase(const PersistArgs &pa, const StreamTab
     if constexpr (XS) {
         if (a.ln_x) {
             // input LayerNorm of the float32 residual rows, straight into shared memory
-            layernorm_rows_to_smem(a, xs, px, s_sum, threadIdx.x, warp, lane);
+            layernorm_rows_to_smem<8>(a, xs, px, s_sum, threadIdx.x, warp, lane);
         } else {
             // stage the M activation rows once for the whole phase
             const int rowv = K / 8, total = M * rowv;

@@ -110,6 +110,26 @@ cudaError_t launch_gemm_tc(const void *map_x, const void *map_w, const LinearArg
                            cudaStream_t s);
 constexpr int kTcMinM = 128;        // prefill linears with at least this many tokens use it
 
+// Decode linear on the tensor cores (tcgen05 / TMEM / TMA): W is the 128-row
+// A operand, the M <= 256 tokens the N operand (NT = gemv_tc_nt(M) columns).
+// map_w: W [N][K] with box rows gemv_tc_box_rows_w(); map_x: x [>= M][K] with
+// box rows NT.  splits > 1 (K split over CTAs) needs part (gemv_tc_part_floats
+// floats) and ticket (one int per 128-row tile, zero at rest); not for ARGMAX.
+struct GemvTcArgs {
+    LinearArgs a;
+    int splits = 1;
+    float *part = nullptr;
+    int *ticket = nullptr;
+};
+constexpr int kTcDecodeMinM = 8;    // decode linears with at least this many tokens use it
+int gemv_tc_nt(int M);
+int gemv_tc_splits(int N, int K, int num_sms, int epi);
+size_t gemv_tc_part_floats(int N, int K, int M, int num_sms);
+int gemv_tc_box_rows_w();
+cudaError_t gemv_tc_prepare();
+cudaError_t launch_gemv_tc(const void *map_w, const void *map_x, const GemvTcArgs &g, int nt,
+                           cudaStream_t s);
+
 // Library-internal host helpers (defined with the C ABI): set the message of
 // bloom_last_error(), and the SM count of the current device.
 void bloom_set_error(const char *fmt, ...);

@@ -84,6 +84,73 @@ __device__ __forceinline__ void tile_epilogue(const LinearArgs &a, const float (
     }
 }
 
+// LayerNorm of the M float32 rows a.ln_x[M][K] into shared memory as bf16
+// (row pitch px bytes), the register-lean form for kernels whose occupancy
+// matters more than the latency of the prologue: float32 statistics, biased
+// variance, eps inside the square root.  Rows are spread over the CTA's warps (a team of 256 / rows
+// threads per row, at least one warp); the statistics come from one pass of
+// sums shifted by the row's first element (sum (x-s), sum (x-s)^2), which keeps
+// the variance free of cancellation when |mean| >> std.  All threads of the CTA
+// call it (two barriers).
+__device__ __forceinline__ void layernorm_rows_to_smem_shifted(const LinearArgs &a, unsigned char *xs,
+                                                       int px, float *s_sum, int tid, int warp,
+                                                       int lane) {
+    const int nthr = blockDim.x, nw = nthr / 32;
+    int team_w = nw;                        // warps per row
+    while (team_w > 1 && team_w > nw / (a.M < nw ? a.M : nw)) team_w >>= 1;
+    const int teams = nw / team_w;
+    const int team = warp / team_w, tw = warp % team_w;
+    const int tthr = team_w * 32, ttid = tw * 32 + lane;
+    float *stat = s_sum;                    // [nw][2]
+    for (int m0 = 0; m0 < a.M; m0 += teams) {
+        const int m = m0 + team;
+        float s1 = 0.f, s2 = 0.f, shift = 0.f;
+        if (m < a.M) {
+            const float *xr = a.ln_x + (size_t)m * a.K;
+            shift = xr[0];
+            for (int k = ttid * 4; k < a.K; k += 4 * tthr) {
+                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+                const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
+                s1 += (d0 + d1) + (d2 + d3);
+                s2 += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+            }
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        if (lane == 0) {
+            stat[2 * warp] = s1;
+            stat[2 * warp + 1] = s2;
+        }
+        __syncthreads();
+        if (m < a.M) {
+            float t1 = 0.f, t2 = 0.f;
+            for (int w = team * team_w; w < (team + 1) * team_w; ++w) {
+                t1 += stat[2 * w];
+                t2 += stat[2 * w + 1];
+            }
+            const float inv_k = 1.f / (float)a.K;
+            const float dm = t1 * inv_k;
+            const float var = fmaxf(t2 * inv_k - dm * dm, 0.f);
+            const float mean = shift + dm;
+            const float rstd = rsqrtf(var + a.ln_eps);
+            const float *xr = a.ln_x + (size_t)m * a.K;
+            uint16_t *dst = reinterpret_cast<uint16_t *>(xs + (size_t)m * px);
+            for (int k = ttid * 4; k < a.K; k += 4 * tthr) {
+                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
+                const uint2 gg = *reinterpret_cast<const uint2 *>(a.ln_g + k);
+                const uint2 bb = *reinterpret_cast<const uint2 *>(a.ln_b + k);
+                uint2 o;
+                o.x = pack_bf2((v.x - mean) * rstd * bf_lo(gg.x) + bf_lo(bb.x),
+                               (v.y - mean) * rstd * bf_hi(gg.x) + bf_hi(bb.x));
+                o.y = pack_bf2((v.z - mean) * rstd * bf_lo(gg.y) + bf_lo(bb.y),
+                               (v.w - mean) * rstd * bf_hi(gg.y) + bf_hi(bb.y));
+                *reinterpret_cast<uint2 *>(dst + k) = o;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // Merge of two (count, mean, sum of squared deviations) summaries of a set of
 // values (the pairwise update of Chan, Golub and LeVeque).
 __device__ __forceinline__ void stats_merge(float &n, float &mean, float &m2, float nb, float meanb,
@@ -112,10 +179,10 @@ __device__ __forceinline__ void stats_merge(float &n, float &mean, float &m2, fl
 // summaries are merged pairwise (no E[x^2] - mean^2 cancellation); the gamma /
 // beta lines are pulled into L1 meanwhile, so that the normalising pass, which
 // re-reads the row from L1, waits on nothing.  All threads of the CTA call it.
+template <int UL>   // float4 loads in flight per thread (register budget of the caller)
 __device__ __forceinline__ void layernorm_rows_to_smem(const LinearArgs &a, unsigned char *xs,
                                                        int px, float *s_sum, int tid, int warp,
                                                        int lane) {
-    constexpr int UL = 8;                   // float4 loads in flight per thread
     const int nthr = blockDim.x, nw = nthr / 32;
     int team_w = nw;                        // warps per row
     while (team_w > 1 && team_w > nw / (a.M < nw ? a.M : nw)) team_w >>= 1;
@@ -174,16 +241,31 @@ __device__ __forceinline__ void layernorm_rows_to_smem(const LinearArgs &a, unsi
             const float rstd = rsqrtf(var + a.ln_eps);
             const float *xr = a.ln_x + (size_t)m * a.K;
             uint16_t *dst = reinterpret_cast<uint16_t *>(xs + (size_t)m * px);
-            for (int k = ttid * 4; k < a.K; k += 4 * tthr) {
-                const float4 v = *reinterpret_cast<const float4 *>(xr + k);
-                const uint2 gg = *reinterpret_cast<const uint2 *>(a.ln_g + k);
-                const uint2 bb = *reinterpret_cast<const uint2 *>(a.ln_b + k);
-                uint2 o;
-                o.x = pack_bf2((v.x - tmean) * rstd * bf_lo(gg.x) + bf_lo(bb.x),
-                               (v.y - tmean) * rstd * bf_hi(gg.x) + bf_hi(bb.x));
-                o.y = pack_bf2((v.z - tmean) * rstd * bf_lo(gg.y) + bf_lo(bb.y),
-                               (v.w - tmean) * rstd * bf_hi(gg.y) + bf_hi(bb.y));
-                *reinterpret_cast<uint2 *>(dst + k) = o;
+            for (int kb = ttid * 4; kb < a.K; kb += 4 * tthr * UL) {
+                // every load of this round first, then the arithmetic
+                float4 v[UL];
+                uint2 gg[UL], bb[UL];
+#pragma unroll
+                for (int u = 0; u < UL; ++u) {
+                    const int k = kb + u * 4 * tthr;
+                    if (k < a.K) {
+                        v[u] = *reinterpret_cast<const float4 *>(xr + k);
+                        gg[u] = __ldg(reinterpret_cast<const uint2 *>(a.ln_g + k));
+                        bb[u] = __ldg(reinterpret_cast<const uint2 *>(a.ln_b + k));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < UL; ++u) {
+                    const int k = kb + u * 4 * tthr;
+                    if (k < a.K) {
+                        uint2 o;
+                        o.x = pack_bf2((v[u].x - tmean) * rstd * bf_lo(gg[u].x) + bf_lo(bb[u].x),
+                                       (v[u].y - tmean) * rstd * bf_hi(gg[u].x) + bf_hi(bb[u].x));
+                        o.y = pack_bf2((v[u].z - tmean) * rstd * bf_lo(gg[u].y) + bf_lo(bb[u].y),
+                                       (v[u].w - tmean) * rstd * bf_hi(gg[u].y) + bf_hi(bb[u].y));
+                        *reinterpret_cast<uint2 *>(dst + k) = o;
+                    }
+                }
             }
         }
         __syncthreads();

@@ -63,8 +63,9 @@ enum {
                                  waits for the previous one to finish before it starts) */
     BLOOM_FLAG_NO_LN_FUSION = 4, /* run every LayerNorm as its own kernel instead of inside
                                     the decode linear kernel that consumes it */
-    BLOOM_FLAG_NO_TC_GEMM = 8,   /* prefill linears of >= 128 tokens on the weight-streaming
-                                    kernel instead of the tensor-core (tcgen05) GEMM */
+    BLOOM_FLAG_NO_TC_GEMM = 8,   /* every linear on the weight-streaming kernel instead of the
+                                    tensor-core (tcgen05) kernels: the prefill GEMM (>= 128
+                                    tokens) and the decode linear (>= 8 sequences) */
     BLOOM_FLAG_PERSISTENT = 16   /* decode steps of <= 16 sequences as one persistent
                                     cooperative launch (all layers as phases separated by grid
                                     barriers) instead of one launch per operation replayed as a
@@ -255,6 +256,16 @@ bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *
  * describe the operands for TMA. */
 bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, int32_t M, int32_t N,
                            int32_t K, int32_t epilogue, void *y, void *stream);
+
+/* The same linear layer on the tensor-core decode kernel that decode steps of
+ * 8 or more sequences use: W is the 128-row operand of tcgen05.mma, the M <= 256
+ * tokens its N operand, both moved by TMA, the accumulator in TMEM; narrow
+ * matrices split K over several CTAs and the last split sums the partials in
+ * split order ("DeepSpeed Inference", III.A: small-batch cost is reading W).
+ * bf16 weights only; x and lin->w 16-byte aligned; K % 8 == 0.  Same
+ * epilogues and result layout as bloom_op_linear. */
+bloom_status bloom_op_linear_tc(const bloom_linear *lin, const void *x, int32_t M, int32_t N,
+                                int32_t K, int32_t epilogue, void *y, void *stream);
 
 /* Split-KV decode attention for one token per sequence.
  * q bf16 [B][n][d]; k_cache, v_cache bf16 [B][n][max_seq][d]; pos int32

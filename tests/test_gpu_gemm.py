@@ -141,3 +141,48 @@ def test_prefill_paths_agree():
         out.append((tok.cpu(), lg.cpu()))
         gm.close()
     assert max_abs(out[0][1], out[1][1].double().numpy()) <= 2e-2
+
+
+# ---------------------------------------------------------------- tensor-core decode linear
+# (M, N, K): every token-column class (16 .. 256), split K (narrow N, long K),
+# ragged N and K tails, one token.
+DECODE_SHAPES = [(8, 3072, 1024), (1, 300, 192), (17, 520, 1000), (64, 4096, 4096),
+                 (130, 1040, 2048), (256, 256, 16384), (16, 12288, 4096), (33, 128, 64)]
+
+
+@pytest.mark.parametrize("M,N,K", DECODE_SHAPES)
+@pytest.mark.parametrize("epi", [bg.EPI_STORE, bg.EPI_GELU, bg.EPI_RESID],
+                         ids=["store", "gelu", "resid"])
+def test_linear_tc(M, N, K, epi):
+    g = gen(M * 131 + N * 7 + K + epi)
+    W = bf((N, K), g, 0.02)
+    x = bf((M, K), g, 1.0)
+    bias = bf((N,), g, 0.5)
+    y0 = bf((M, N), g, 1.0)
+    acc = oracle.linear(f64(x), oracle.host_bits(W), oracle.host_bits(bias))
+    y = y0.to(DEV).clone()
+    bg.op_linear_tc(x.to(DEV), W.to(DEV), bias=bias.to(DEV), epilogue=epi, y=y)
+    if epi == bg.EPI_STORE:
+        ref = acc
+    elif epi == bg.EPI_GELU:
+        ref = np.vectorize(oracle.gelu)(acc)
+    else:
+        ref = f64(y0) + acc
+    assert_kernel_close(y, ref, what=f"linear_tc {M}x{N}x{K}")
+
+
+def test_linear_tc_deterministic_split_k():
+    """K split over CTAs: partials summed in split order, so repeated runs agree bitwise."""
+    g = gen(77)
+    W = bf((512, 16384), g, 0.02).to(DEV)
+    x = bf((24, 16384), g).to(DEV)
+    y1 = bg.op_linear_tc(x, W)
+    y2 = bg.op_linear_tc(x, W)
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_TC_GEMM], ids=["tcgen05", "streaming"])
+def test_decode_generation_batch16(flags):
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=5000, batch=16)
+    w = synth.make_weights(shape, seed=12, random_affine=True)
+    generate_parity(shape, w, steps=4, tol=2e-2, flags=flags)
