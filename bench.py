@@ -65,26 +65,38 @@ def head_launch_bytes(sh: synth.Shape, B: int) -> int:
 
 
 # ------------------------------------------------------------------ measured DRAM traffic
-HEAD_SOURCES = ["k_linear.cu", "tile_ops.cuh", "common.cuh", "kernels.h"]
+# The LM head + argmax runs on the tensor-core decode kernel from 8 sequences
+# on (unless disabled), else on the weight-streaming kernel.
+HEAD_KERNELS = {
+    "gemv_tc": ("gemv_tc_kernel (tensor-core LM head + argmax)",
+                ["k_gemv_tc.cu", "tc_ops.cuh", "tile_ops.cuh", "common.cuh", "kernels.h"]),
+    "linear": ("linear_kernel (weight-streaming LM head + argmax)",
+               ["k_linear.cu", "tile_ops.cuh", "common.cuh", "kernels.h"]),
+}
+TC_HEAD_MIN_B = 8
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lm_head_traffic.json")
 
 
-def head_source_digest() -> str:
+def head_kernel(B: int, tc: bool) -> str:
+    return "gemv_tc" if tc and B >= TC_HEAD_MIN_B else "linear"
+
+
+def head_source_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in HEAD_SOURCES:
+    for f in HEAD_KERNELS[kernel][1]:
         with open(os.path.join(ROOT, "bloom_decoder_token_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def head_traffic(sh: synth.Shape, B: int):
+def head_traffic(sh: synth.Shape, B: int, kernel: str):
     """dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch as an
-    ncu capture recorded it for this workload, or None when there is no capture
-    for it or the kernel's sources changed since."""
+    ncu capture recorded it for this workload and kernel, or None when there is
+    no capture for it or the kernel's sources changed since."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    d = json.load(open(TRAFFIC_FILE))
-    if d.get("kernel_source_sha256") != head_source_digest():
+    d = json.load(open(TRAFFIC_FILE)).get("kernels", {}).get(kernel)
+    if not d or d.get("kernel_source_sha256") != head_source_digest(kernel):
         return None
     return d.get("bytes_per_launch", {}).get(f"{sh.name}/B{B}")
 
@@ -117,13 +129,15 @@ def run_roofline_only(args, sh):
     torch.cuda.set_device(dev)
     B = sh.batch
     w = synth.make_weights(sh.with_(n_layer=1), seed=0, device=dev)
-    gm = bg.Model(w, max_batch=B, max_tokens=B * sh.prompt, max_seq=sh.max_seq)
+    gm = bg.Model(w, max_batch=B, max_tokens=B * sh.prompt, max_seq=sh.max_seq,
+                  flags=bg.FLAG_NO_TC_GEMM if args.no_tc_gemm else 0)
+    kernel = head_kernel(B, not args.no_tc_gemm)
     head_ms, head_bytes, head_gbs = measure_head(gm, sh, B, dev, torch.cuda.current_stream(dev))
     hbm, src = peaks()
-    print(json.dumps({"roofline_only": True, "workload": f"{sh.name}/B{B}", "launch_ms": head_ms,
-                      "bytes_per_launch": head_bytes, "achieved_gbs": head_gbs,
-                      "frac": head_gbs / hbm, "peak_source": src,
-                      "kernel_source_sha256": head_source_digest()}), flush=True)
+    print(json.dumps({"roofline_only": True, "workload": f"{sh.name}/B{B}", "kernel": kernel,
+                      "launch_ms": head_ms, "bytes_per_launch": head_bytes,
+                      "achieved_gbs": head_gbs, "frac": head_gbs / hbm, "peak_source": src,
+                      "kernel_source_sha256": head_source_digest(kernel)}), flush=True)
     gm.close()
 
 
@@ -328,7 +342,8 @@ def run_ours(args, sh):
     dec_gbs = step_bytes / (dec_ms / 1e3) / 1e9
 
     head_ms, head_bytes, head_gbs = measure_head(gm, sh, B, dev, stream)
-    traffic = args.head_traffic if args.head_traffic is not None else head_traffic(sh, B)
+    kernel = head_kernel(B, not args.no_tc_gemm)
+    traffic = args.head_traffic if args.head_traffic is not None else head_traffic(sh, B, kernel)
 
     # end to end through the public API with host buffers
     ids_h = ids.contiguous().pin_memory()
@@ -378,7 +393,7 @@ def run_ours(args, sh):
             "decode_step_bytes": step_bytes,
             "decode_hbm_gbs": dec_gbs,
             "decode_hbm_frac": dec_gbs / hbm,
-            "roofline": {"bound": "hbm", "kernel": "linear_kernel (tied LM head + argmax)",
+            "roofline": {"bound": "hbm", "kernel": HEAD_KERNELS[kernel][0],
                          "achieved": head_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": head_gbs / hbm, "traffic": traffic,
                          "peak_source": src, "bytes_per_launch": head_bytes,

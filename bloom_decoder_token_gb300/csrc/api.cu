@@ -91,7 +91,7 @@ struct TcMap {
     alignas(64) unsigned char b[128];
 };
 enum { TC_QKV = 0, TC_O = 1, TC_UP = 2, TC_DOWN = 3, TC_PER_LAYER = 4 };
-enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2, TC_X_XL = 3 };
+enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2 };
 constexpr int kTcNtClasses = 5;   // decode token columns 16, 32, 64, 128, 256
 
 // Phase table of the persistent decode step for one set of step buffers.
@@ -132,14 +132,11 @@ struct bloom_model {
     bool tc = false;
     std::vector<TcMap> wmaps;
     TcMap xmaps[3];
-    // tensor-core decode linear: weight maps (box 128 rows) [layer][TC_*] then the
-    // head; activation maps [TC_X_*][token-column class]; split-K scratch
+    // tensor-core LM head (decode steps of >= kTcDecodeMinM sequences): the
+    // embedding's map (box 128 rows) and the ln_f output's maps per token-column class
     bool tcd = false;
-    std::vector<TcMap> dwmaps;
-    TcMap dxmaps[4][kTcNtClasses];
-    void *gv_scratch = nullptr;
-    float *gv_part = nullptr;
-    int *gv_ticket = nullptr;
+    TcMap head_wmap;
+    TcMap head_xmaps[kTcNtClasses];
     // persistent decode step: grid (0 = not available), barrier words, phase tables
     int pgrid = 0;
     int pmax_phases = 0;
@@ -200,7 +197,6 @@ extern "C" bloom_status bloom_destroy(bloom_model *m) {
     for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
     for (auto &p : m->plans) cudaFree(p.phases);
     if (m->pscratch) cudaFree(m->pscratch);
-    if (m->gv_scratch) cudaFree(m->gv_scratch);
     if (m->cap) cudaStreamDestroy(m->cap);
     if (m->ws) cudaFree(m->ws);
     delete m;
@@ -297,46 +293,19 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         linear_prepare() != cudaSuccess) {
         st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
     }
-    // decode linears of >= kTcDecodeMinM tokens on the tensor cores
-    if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_batch >= kTcDecodeMinM) {
-        bool ok = gemm_map_bytes() == sizeof(TcMap);
-        const int bw = gemv_tc_box_rows_w();
-        m->dwmaps.resize((size_t)cfg->n_layer * TC_PER_LAYER + 1);
-        for (int l = 0; ok && l < cfg->n_layer; ++l) {
-            const bloom_layer_weights &L = w->layers[l];
-            TcMap *wm = &m->dwmaps[(size_t)l * TC_PER_LAYER];
-            ok = gemm_make_map(wm[TC_QKV].b, L.qkv.w, 3 * h, h, bw) &&
-                 gemm_make_map(wm[TC_O].b, L.o.w, h, h, bw) &&
-                 gemm_make_map(wm[TC_UP].b, L.up.w, F, h, bw) &&
-                 gemm_make_map(wm[TC_DOWN].b, L.down.w, h, F, bw);
-        }
-        ok = ok && gemm_make_map(m->dwmaps.back().b, w->word_emb, cfg->vocab, h, bw);
+    // the LM head of decode steps of >= kTcDecodeMinM sequences on the tensor cores
+    if (!st2 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_batch >= kTcDecodeMinM) {
+        bool ok = gemm_map_bytes() == sizeof(TcMap) &&
+                  gemm_make_map(m->head_wmap.b, w->word_emb, cfg->vocab, h, gemv_tc_box_rows_w());
         const int ntmax = gemv_tc_nt(cfg->max_batch);
-        for (int ci = 0; ok && ci < kTcNtClasses && (16 << ci) <= ntmax; ++ci) {
-            const int nt = 16 << ci;
-            ok = gemm_make_map(m->dxmaps[TC_X_A][ci].b, m->a, cfg->max_batch, h, nt) &&
-                 gemm_make_map(m->dxmaps[TC_X_O][ci].b, m->o, cfg->max_batch, h, nt) &&
-                 gemm_make_map(m->dxmaps[TC_X_U][ci].b, m->u, cfg->max_batch, F, nt) &&
-                 gemm_make_map(m->dxmaps[TC_X_XL][ci].b, m->xl, cfg->max_batch, h, nt);
-        }
-        size_t part = 0;
-        const int shapes[4][2] = {{3 * h, h}, {h, h}, {F, h}, {h, F}};
-        for (auto &nk : shapes)
-            part = std::max(part, gemv_tc_part_floats(nk[0], nk[1], cfg->max_batch, m->num_sms));
-        const size_t tickets = (size_t)(std::max(3 * h, F) + 127) / 128;
-        const size_t pb = align256(part * 4), bytes = pb + tickets * 4;
-        if (!ok) {
-            st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the decode linears could not be encoded");
-        } else if (gemv_tc_prepare() != cudaSuccess) {
-            st2 = fail(BLOOM_E_CUDA, "decode linear setup: %s", cudaGetErrorString(cudaGetLastError()));
-        } else if (cudaMalloc(&m->gv_scratch, bytes) != cudaSuccess ||
-                   cudaMemset(m->gv_scratch, 0, bytes) != cudaSuccess) {
-            st2 = fail(BLOOM_E_OOM, "decode linear scratch of %zu bytes", bytes);
-        } else {
-            m->gv_part = (float *)m->gv_scratch;
-            m->gv_ticket = (int *)((char *)m->gv_scratch + pb);
+        for (int ci = 0; ok && ci < kTcNtClasses && (16 << ci) <= ntmax; ++ci)
+            ok = gemm_make_map(m->head_xmaps[ci].b, m->xl, cfg->max_batch, h, 16 << ci);
+        if (!ok)
+            st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the LM head could not be encoded");
+        else if (gemv_tc_prepare() != cudaSuccess)
+            st2 = fail(BLOOM_E_CUDA, "LM head setup: %s", cudaGetErrorString(cudaGetLastError()));
+        else
             m->tcd = true;
-        }
     }
     if (!st2 && (cfg->flags & BLOOM_FLAG_PERSISTENT)) {
         m->pgrid = persist_grid(i8);   // 0: no cooperative launch of one block per SM here
@@ -456,33 +425,33 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
 
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
 // kTcMinM tokens or more, else the weight-streaming kernel.
-// Decode linear on the tensor cores; wmap_index into dwmaps, xmap one of TC_X_*.
-static cudaError_t run_gemv_tc(bloom_model *m, const LinearArgs &a, size_t wmap_index, int xmap,
-                               cudaStream_t s) {
+// The LM head + argmax on the tensor cores (one pass over the embedding; no K split).
+static bool use_tc_head(const bloom_model *m, const LinearArgs &a) {
+    return m->tcd && a.epi == EPI_ARGMAX && a.M >= kTcDecodeMinM && a.M <= m->cfg.max_batch &&
+           !a.ln_x;
+}
+
+static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t s) {
     const int nt = gemv_tc_nt(a.M);
     int ci = 0;
     while ((16 << ci) < nt) ++ci;
     GemvTcArgs g;
     g.a = a;
-    g.splits = gemv_tc_splits(a.N, a.K, m->num_sms, a.epi);
-    g.part = m->gv_part;
-    g.ticket = m->gv_ticket;
-    return launch_gemv_tc(m->dwmaps[wmap_index].b, m->dxmaps[xmap][ci].b, g, nt, s);
-}
-
-static bool use_gemv_tc(const bloom_model *m, const LinearArgs &a) {
-    return m->tcd && a.T == 0 && a.M >= kTcDecodeMinM && a.M <= m->cfg.max_batch && !a.ln_x &&
-           !a.int8;
+    g.splits = 1;
+    return launch_gemv_tc(m->head_wmap.b, m->head_xmaps[ci].b, g, nt, s);
 }
 
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
-// kTcMinM tokens or more, the tensor-core decode linear for kTcDecodeMinM
-// tokens or more, else the weight-streaming kernel.
+// kTcMinM tokens or more, else the weight-streaming kernel.  Decode block
+// linears stay on the weight-streaming kernel at every batch: measured in whole
+// decode steps, its small shared-memory footprint lets the next kernel's CTAs
+// start under the previous one's tail (programmatic dependent launch), which
+// outweighs the tensor-core kernel's faster stream on 2-134 MB matrices (the
+// tensor-core decode linear serves the LM head, enqueue_head).
 static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wmap, int xmap,
                               cudaStream_t s) {
     if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x)
         return launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
-    if (use_gemv_tc(m, a)) return run_gemv_tc(m, a, (size_t)l * TC_PER_LAYER + wmap, xmap, s);
     return launch_linear(a, m->num_sms, s);
 }
 
@@ -598,7 +567,7 @@ static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int strid
                                          B, c.hidden, c.ln_eps, m->xl, stride, last, s))) {
         return e;
     }
-    if (use_gemv_tc(m, a)) return run_gemv_tc(m, a, m->dwmaps.size() - 1, TC_X_XL, s);
+    if (use_tc_head(m, a)) return run_tc_head(m, a, s);
     return launch_linear(a, m->num_sms, s);
 }
 
@@ -1007,6 +976,17 @@ extern "C" bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B,
     a.best = m->best;
     a.ticket = m->head_ticket;
     a.out_tokens = out_tokens;
+    if (use_tc_head(m, a)) {
+        // the decode step's kernel for this batch: a TMA descriptor of the caller's rows
+        const int nt = gemv_tc_nt(B);
+        TcMap mx;
+        if (!gemm_make_map(mx.b, xn, B, m->cfg.hidden, nt))
+            return fail(BLOOM_E_UNSUPPORTED, "TMA descriptor of xn could not be encoded");
+        GemvTcArgs g;
+        g.a = a;
+        CK(launch_gemv_tc(m->head_wmap.b, mx.b, g, nt, (cudaStream_t)stream));
+        return BLOOM_OK;
+    }
     CK(launch_linear(a, m->num_sms, (cudaStream_t)stream));
     return BLOOM_OK;
 }

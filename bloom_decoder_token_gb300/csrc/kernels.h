@@ -121,7 +121,7 @@ struct GemvTcArgs {
     float *part = nullptr;
     int *ticket = nullptr;
 };
-constexpr int kTcDecodeMinM = 8;    // decode linears with at least this many tokens use it
+constexpr int kTcDecodeMinM = 8;    // decode steps of at least this many sequences: LM head on it
 int gemv_tc_nt(int M);
 int gemv_tc_splits(int N, int K, int num_sms, int epi);
 size_t gemv_tc_part_floats(int N, int K, int M, int num_sms);

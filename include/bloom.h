@@ -65,7 +65,7 @@ enum {
                                     the decode linear kernel that consumes it */
     BLOOM_FLAG_NO_TC_GEMM = 8,   /* every linear on the weight-streaming kernel instead of the
                                     tensor-core (tcgen05) kernels: the prefill GEMM (>= 128
-                                    tokens) and the decode linear (>= 8 sequences) */
+                                    tokens) and the decode LM head (>= 8 sequences) */
     BLOOM_FLAG_PERSISTENT = 16   /* decode steps of <= 16 sequences as one persistent
                                     cooperative launch (all layers as phases separated by grid
                                     barriers) instead of one launch per operation replayed as a
@@ -257,8 +257,9 @@ bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *
 bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, int32_t M, int32_t N,
                            int32_t K, int32_t epilogue, void *y, void *stream);
 
-/* The same linear layer on the tensor-core decode kernel that decode steps of
- * 8 or more sequences use: W is the 128-row operand of tcgen05.mma, the M <= 256
+/* The same linear layer on the tensor-core decode kernel (the LM head of
+ * decode steps of 8 or more sequences runs on it): W is the 128-row operand of
+ * tcgen05.mma, the M <= 256
  * tokens its N operand, both moved by TMA, the accumulator in TMEM; narrow
  * matrices split K over several CTAs and the last split sums the partials in
  * split order ("DeepSpeed Inference", III.A: small-batch cost is reading W).
