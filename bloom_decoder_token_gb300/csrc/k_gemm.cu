@@ -6,19 +6,22 @@
 // so they run as 128 x 256 output tiles on the tensor cores instead of
 // streaming the weights per token tile.
 //
-// One CTA computes one 128 (tokens) x 256 (features) tile:
+// One CTA per SM walks the 128 (tokens) x 256 (features) output tiles
+// (persistent), with two accumulators in TMEM so that the epilogue of one tile
+// overlaps the main loop of the next:
 //  * warp 0, one lane: TMA producer.  Two 2-D tensor maps (128B swizzle) move
 //    a 128 x 64 tile of X and a 256 x 64 tile of W per k-block into a 4-stage
 //    shared-memory ring, completing an mbarrier per stage;
 //  * warp 1, one lane: issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32,
-//    M = 128, N = 256, K = 16 per instruction, 4 per k-block) into a TMEM
-//    accumulator of 256 columns, and tcgen05.commit frees each stage when its
-//    MMAs are done; a last commit signals the accumulator complete;
+//    M = 128, N = 256, K = 16 per instruction, 4 per k-block) into one of two
+//    TMEM accumulators of 256 columns (the SM's 512), once the epilogue has
+//    drained it; tcgen05.commit frees each stage when its MMAs are done and
+//    signals each tile's accumulator complete;
 //  * warps 2-5: epilogue.  Each warp reads its 32-lane quarter of the
 //    accumulator with tcgen05.ld (lane = token row, 32 columns at a time),
 //    adds the bias and applies GeLU, the float32 residual add or the
 //    head-interleaved Q/K/V scatter into the KV cache ("DeepSpeed Inference",
-//    III.D fusions), and stores.
+//    III.D fusions), stores, and hands the accumulator back to the MMA lane.
 // Warp 0 also allocates and frees the TMEM columns.  Every wait is bounded
 // (about two seconds of SM clock); on expiry the kernel records kErrTimeout,
 // skips its stores, and still frees TMEM.
@@ -115,6 +118,21 @@ __device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[3
     }
 }
 
+// Tile order: groups of kTcGroupM row blocks, row block fastest inside a group,
+// so that the tiles running at once share a few X row blocks and each W tile
+// is used by kTcGroupM neighbouring tiles while it is still in L2.
+constexpr int kTcGroupM = 8;
+
+__device__ __forceinline__ void tc_tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &n0) {
+    const int per_group = kTcGroupM * tiles_n;
+    const int group = t / per_group;
+    const int first = group * kTcGroupM;
+    const int gm = min(kTcGroupM, tiles_m - first);
+    const int r = t - group * per_group;
+    m0 = (first + r % gm) * kTcBM;
+    n0 = (r / gm) * kTcBN;
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -123,29 +141,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     // 1024-byte alignment for the 128B-swizzled tiles
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         ((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t full[kTcStages], empty[kTcStages], acc_full;
+    __shared__ uint64_t full[kTcStages], empty[kTcStages], acc_full[2], acc_empty[2], drained;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.x * kTcBM, n0 = blockIdx.y * kTcBN;
     const int nkb = (a.K + kTcBK - 1) / kTcBK;
+    const int tiles_n = (a.N + kTcBN - 1) / kTcBN;
+    const int tiles_m = (a.M + kTcBM - 1) / kTcBM;
+    const int tiles = tiles_m * tiles_n;
 
     if (tid == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             tc_mbar_init(&full[s], 1);
             tc_mbar_init(&empty[s], 1);
         }
-        tc_mbar_init(&acc_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            tc_mbar_init(&acc_full[b], 1);
+            tc_mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
+        }
+        tc_mbar_init(&drained, 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_x) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_w) : "memory");
     }
     if (warp == 0) {
+        // two accumulators of 256 columns: the whole TMEM of the SM (one CTA per SM)
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          tc_smem(&tmem_base)),
-                     "n"(kTcBN));
+                     "n"(2 * kTcBN));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -153,81 +178,116 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
     griddep_launch();
+    volatile int *abort_flag = &s_abort;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer
+            // ---- TMA producer: this CTA's tiles back to back through one ring
             griddep_wait();   // X comes from the previous kernel
-            int issued = 0;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kTcStages;
-                const uint32_t par = (uint32_t)((kb / kTcStages) & 1);
-                if (!tc_mbar_wait(&empty[s], par ^ 1u)) {
-                    s_abort = 1;
-                    if (a.err) atomicOr(a.err, kErrTimeout);
-                    break;
+            long long it = 0;   // ring position over all tiles
+            for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+                int m0, n0;
+                tc_tile_coords(t, tiles_m, tiles_n, m0, n0);
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = (int)(it % kTcStages);
+                    const uint32_t par = (uint32_t)((it / kTcStages) & 1);
+                    if (!tc_mbar_wait(&empty[s], par ^ 1u)) {
+                        *abort_flag = 1;
+                        if (a.err) atomicOr(a.err, kErrTimeout);
+                        break;
+                    }
+                    unsigned char *sa = smem + (size_t)s * kTcStageBytes;
+                    unsigned char *sb = sa + kTcABytes;
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                                     tc_smem(&full[s])),
+                                 "r"(kTcStageBytes)
+                                 : "memory");
+                    tc_tma_2d(sa, &tm_x, kb * kTcBK, m0, &full[s]);
+                    tc_tma_2d(sb, &tm_w, kb * kTcBK, n0, &full[s]);
                 }
-                unsigned char *sa = smem + (size_t)s * kTcStageBytes;
-                unsigned char *sb = sa + kTcABytes;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                                 tc_smem(&full[s])),
-                             "r"(kTcStageBytes)
-                             : "memory");
-                tc_tma_2d(sa, &tm_x, kb * kTcBK, m0, &full[s]);
-                tc_tma_2d(sb, &tm_w, kb * kTcBK, n0, &full[s]);
-                ++issued;
             }
             // no copy of ours may still be landing when the CTA exits
-            for (int i = 0; i < kTcStages && i < issued; ++i) {
-                const int kb = issued - 1 - i;
-                if (!tc_mbar_wait(&full[kb % kTcStages], (uint32_t)((kb / kTcStages) & 1)))
+            for (int i = 0; i < kTcStages && i < it; ++i) {
+                const long long j = it - 1 - i;
+                if (!tc_mbar_wait(&full[j % kTcStages], (uint32_t)((j / kTcStages) & 1)))
                     if (a.err) atomicOr(a.err, kErrTimeout);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---- MMA issuer
+            // ---- MMA issuer: tile i accumulates into TMEM buffer i % 2 once the
+            // epilogue has drained that buffer's previous tile
             constexpr uint32_t idesc = tc_idesc(kTcBM, kTcBN);
+            long long it = 0;
+            int lt = 0;
             bool ok = true;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kTcStages;
-                const uint32_t par = (uint32_t)((kb / kTcStages) & 1);
-                if (!tc_mbar_wait(&full[s], par)) {
+            for (int t = blockIdx.x; t < tiles && ok && !*abort_flag; t += gridDim.x, ++lt) {
+                const int b = lt & 1;
+                if (!tc_mbar_wait(&acc_empty[b], (uint32_t)(((lt >> 1) & 1) ^ 1))) {
                     ok = false;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t sa = tc_smem(smem + (size_t)s * kTcStageBytes);
-                const uint32_t sb = sa + kTcABytes;
-                const uint64_t da = tc_desc(sa), db = tc_desc(sb);
+                const uint32_t acc = tmem + (uint32_t)(b * kTcBN);
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = (int)(it % kTcStages);
+                    if (!tc_mbar_wait(&full[s], (uint32_t)((it / kTcStages) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t sa = tc_smem(smem + (size_t)s * kTcStageBytes);
+                    const uint32_t sb = sa + kTcABytes;
+                    const uint64_t da = tc_desc(sa), db = tc_desc(sb);
 #pragma unroll
-                for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes per step
-                    tc_mma(tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc,
-                           (kb > 0 || k > 0) ? 1u : 0u);
-                tc_commit(&empty[s]);   // stage free once these MMAs have read it
+                    for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes per step
+                        tc_mma(acc, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc,
+                               (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(&empty[s]);   // stage free once these MMAs have read it
+                }
+                tc_commit(&acc_full[b]);    // this tile's accumulator complete (or abandoned)
             }
             if (!ok) {
-                s_abort = 1;
+                *abort_flag = 1;
                 if (a.err) atomicOr(a.err, kErrTimeout);
             }
-            tc_commit(&acc_full);       // accumulator complete (or abandoned)
+            // every MMA of ours has finished before TMEM is freed, on every path
+            tc_commit(&drained);
+            if (!tc_mbar_wait(&drained, 0) && a.err) atomicOr(a.err, kErrTimeout);
         }
     } else {
         // ---- epilogue: warps 2..5 -> TMEM lane quarters (warp % 4)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const int m = m0 + row;
         griddep_wait();   // the residual and the cache belong to earlier kernels too
-        // longer limit than the MMA issuer's, so that its final commit arrives first
-        const bool ok = tc_mbar_wait(&acc_full, 0, 3 * kTcWaitCycles);
-        if (!ok) if (a.err) atomicOr(a.err, kErrTimeout);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const bool store = ok && !*(volatile int *)&s_abort && m < a.M;
+        int lt = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+            const int b = lt & 1;
+            int m0, n0;
+            tc_tile_coords(t, tiles_m, tiles_n, m0, n0);
+            const int m = m0 + row;
+            // longer limit than the MMA issuer's, so that its commits arrive first
+            const bool ok = tc_mbar_wait(&acc_full[b], (uint32_t)((lt >> 1) & 1), 3 * kTcWaitCycles);
+            if (!ok) {
+                if (a.err) atomicOr(a.err, kErrTimeout);
+                *abort_flag = 1;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const bool store = !*abort_flag && m < a.M;
+            const uint32_t acc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kTcBN);
 #pragma unroll 1
-        for (int c = 0; c < kTcBN; c += 32) {
-            float v[32];
-            tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);   // whole warp
-            if (store && n0 + c < a.N) tc_store_chunk<EPI>(a, v, m, n0 + c);
+            for (int c = 0; c < kTcBN; c += 32) {
+                float v[32];
+                tc_ld32(acc + (uint32_t)c, v);   // whole warp
+                if (store && n0 + c < a.N) tc_store_chunk<EPI>(a, v, m, n0 + c);
+            }
+            // buffer b drained: the MMA issuer may start the tile after next in it
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&acc_empty[b]))
+                             : "memory");
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -235,7 +295,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "n"(kTcBN));
+                     "n"(2 * kTcBN));
     }
 }
 
@@ -289,7 +349,16 @@ static cudaError_t gemm_launch_t(const void *mx, const void *mw, const LinearArg
     }
     const CUtensorMap &tx = *reinterpret_cast<const CUtensorMap *>(mx);
     const CUtensorMap &tw = *reinterpret_cast<const CUtensorMap *>(mw);
-    dim3 grid((a.M + kTcBM - 1) / kTcBM, (a.N + kTcBN - 1) / kTcBN);
+    // persistent: one CTA per SM walks the tiles
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ||
+            sms < 1)
+            sms = 1;
+    }
+    const long long tiles = (long long)((a.M + kTcBM - 1) / kTcBM) * ((a.N + kTcBN - 1) / kTcBN);
+    dim3 grid((unsigned)(tiles < sms ? tiles : sms));
     return launch_pdl_smem(gemm_tc_kernel<EPI>, grid, dim3(kTcThreads), kTcSmem, s, tx, tw, a);
 }
 
