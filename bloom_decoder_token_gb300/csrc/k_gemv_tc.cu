@@ -219,7 +219,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         const bool ok = tc_mbar_wait(&acc_full, 0, 3 * kTcWaitCycles);
         if (!ok && a.err) atomicOr(a.err, kErrTimeout);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const bool live = ok && !*(volatile int *)&s_abort;
+        // warp-uniform, so that the argmax shuffles below see every lane
+        const bool live = __all_sync(0xffffffffu, ok && !*(volatile int *)&s_abort);
         const int mmax = a.M < NT ? a.M : NT;
         const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
         if (g.splits == 1) {
