@@ -54,6 +54,24 @@ __device__ __forceinline__ uint4 ld_act(const void *p) {
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// ---- asynchronous global -> shared copies (one 16-byte piece per call) ----
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ---- reductions ----
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

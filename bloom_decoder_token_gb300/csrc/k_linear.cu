@@ -41,13 +41,33 @@ namespace bloom {
 constexpr int kLinWarps = 8;
 constexpr int kLinThreads = kLinWarps * kWarp;
 
-template <int MT, bool INT8, int EPI, bool LNF>
+// Output element e (0..3) of lane (g, q)'s accumulator tile mt: token m and
+// weight row n.  Weights as the B operand (WA = false): 8 rows x 16 tokens;
+// as the A operand (WA = true): 16 rows x 8 tokens.
+template <bool WA>
+__device__ __forceinline__ void tile_elem(int e, int mt, int m0, int row0, int g, int q, int &m,
+                                          int &n) {
+    if constexpr (WA) {
+        m = m0 + mt * 8 + 2 * q + (e & 1);
+        n = row0 + g + 8 * (e >> 1);
+    } else {
+        m = m0 + mt * 16 + g + 8 * (e >> 1);
+        n = row0 + 2 * q + (e & 1);
+    }
+}
+
+template <int MT, bool INT8, int EPI, bool LNF, bool WA>
 __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a) {
     constexpr int EPL = INT8 ? 16 : 8;   // weights per lane per chunk (16 bytes)
     constexpr int KC = 4 * EPL;          // k per chunk
     constexpr int NS = EPL / 4;          // mma k-steps per chunk
     constexpr int XW = EPL / 2;          // 32-bit words of x per lane per chunk
     constexpr int U = (MT >= 4) ? 2 : 4; // chunks in flight per warp
+    constexpr int RG = WA ? 16 : 8;      // weight rows per task
+    constexpr int TT = WA ? 8 * MT : 16 * MT;   // tokens per task
+    constexpr int NR = WA ? 2 : 1;       // weight rows a lane loads (g, g + 8)
+    // int8 as the A operand: weights a few batches ahead are pulled towards L2
+    constexpr int PF = (WA && INT8) ? 2 : 0;
 
     extern __shared__ __align__(16) unsigned char xs[];   // LNF: [M][K*2 + 64] bf16
     __shared__ float red[kLinWarps][MT][4][kWarp];
@@ -63,8 +83,8 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     }
 
     const int nchunks = (a.K + KC - 1) / KC;
-    const int row_groups = (a.N + 7) / 8;
-    const int tok_tiles = (a.M + 16 * MT - 1) / (16 * MT);
+    const int row_groups = (a.N + RG - 1) / RG;
+    const int tok_tiles = (a.M + TT - 1) / TT;
     const long long tasks = (long long)row_groups * tok_tiles;
     const size_t row_bytes = (size_t)a.K * (INT8 ? 1 : 2);
     const char *wbase = reinterpret_cast<const char *>(a.w);
@@ -74,11 +94,14 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
         // pull the first task's weight chunks towards L2 (they depend on no
         // earlier kernel), then wait for x and normalise its rows once
         if (blockIdx.x < tasks && q == 0) {
-            const int wrow = (int)(blockIdx.x / tok_tiles) * 8 + g;
-            if (wrow < a.N)
-                for (int c = warp; c < nchunks && c < 2 * U * kLinWarps; c += kLinWarps)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(
-                        wbase + (size_t)wrow * row_bytes + (size_t)c * KC * (INT8 ? 1 : 2)));
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int wrow = (int)(blockIdx.x / tok_tiles) * RG + g + 8 * r;
+                if (wrow < a.N)
+                    for (int c = warp; c < nchunks && c < 2 * U * kLinWarps; c += kLinWarps)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                            wbase + (size_t)wrow * row_bytes + (size_t)c * KC * (INT8 ? 1 : 2)));
+            }
         }
         griddep_wait();
         waited = true;
@@ -88,10 +111,15 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {
         const int rg = (int)(task / tok_tiles);
         const int tt = (int)(task - (long long)rg * tok_tiles);
-        const int row0 = rg * 8, m0 = tt * 16 * MT;
-        const int wrow = row0 + g;
-        const bool wok = wrow < a.N;
-        const char *wp = wbase + (size_t)(wok ? wrow : 0) * row_bytes + (size_t)q * 16;
+        const int row0 = rg * RG, m0 = tt * TT;
+        bool wok[NR];
+        const char *wp[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const int wrow = row0 + g + 8 * r;
+            wok[r] = wrow < a.N;
+            wp[r] = wbase + (size_t)(wok[r] ? wrow : 0) * row_bytes + (size_t)q * 16;
+        }
         float acc[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -99,14 +127,30 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
             for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
 
         for (int c0 = warp; c0 < nchunks; c0 += kLinWarps * U) {
-            uint4 wv[U];
+            uint4 wv[NR][U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = c0 + u * kLinWarps;
                 const int k = c * KC + q * EPL;
-                wv[u] = (wok && c < nchunks && k < a.K)
-                            ? ld_stream(wp + (size_t)c * KC * (INT8 ? 1 : 2))
-                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    wv[r][u] = (wok[r] && c < nchunks && k < a.K)
+                                   ? ld_stream(wp[r] + (size_t)c * KC * (INT8 ? 1 : 2))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+            if constexpr (PF > 0) {
+                if (q == 0) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + u * kLinWarps + PF * kLinWarps * U;
+                        if (c < nchunks)
+#pragma unroll
+                            for (int r = 0; r < NR; ++r)
+                                if (wok[r])
+                                    asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                                        wp[r] + (size_t)c * KC * (INT8 ? 1 : 2)));
+                    }
+                }
             }
             if (!waited) {
                 griddep_wait();   // x (and the residual) come from earlier kernels
@@ -117,10 +161,11 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
                 const int c = c0 + u * kLinWarps;
                 if (c >= nchunks) break;
                 const int k = c * KC + q * EPL;
-                uint32_t xa[MT][XW], xb[MT][XW];
+                // activation fragments: tokens g (WA) or g, g + 8 of each tile
+                uint32_t xa[MT][XW], xb[MT][WA ? 1 : XW];
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    const int ma = m0 + mt * 16 + g, mb = ma + 8;
+                    const int ma = m0 + mt * (WA ? 8 : 16) + g, mb = ma + 8;
 #pragma unroll
                     for (int hh = 0; hh < XW / 4; ++hh) {
                         uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
@@ -128,34 +173,50 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
                             if (ma < a.M && k < a.K)
                                 va = *reinterpret_cast<const uint4 *>(xs + (size_t)ma * PX +
                                                                       (size_t)(k + 8 * hh) * 2);
-                            if (mb < a.M && k < a.K)
+                            if (!WA && mb < a.M && k < a.K)
                                 vb = *reinterpret_cast<const uint4 *>(xs + (size_t)mb * PX +
                                                                       (size_t)(k + 8 * hh) * 2);
                         } else {
                             if (ma < a.M && k < a.K) va = ld_act(a.x + (size_t)ma * a.K + k + 8 * hh);
-                            if (mb < a.M && k < a.K) vb = ld_act(a.x + (size_t)mb * a.K + k + 8 * hh);
+                            if (!WA && mb < a.M && k < a.K)
+                                vb = ld_act(a.x + (size_t)mb * a.K + k + 8 * hh);
                         }
                         xa[mt][4 * hh + 0] = va.x; xa[mt][4 * hh + 1] = va.y;
                         xa[mt][4 * hh + 2] = va.z; xa[mt][4 * hh + 3] = va.w;
-                        xb[mt][4 * hh + 0] = vb.x; xb[mt][4 * hh + 1] = vb.y;
-                        xb[mt][4 * hh + 2] = vb.z; xb[mt][4 * hh + 3] = vb.w;
+                        if constexpr (!WA) {
+                            xb[mt][4 * hh + 0] = vb.x; xb[mt][4 * hh + 1] = vb.y;
+                            xb[mt][4 * hh + 2] = vb.z; xb[mt][4 * hh + 3] = vb.w;
+                        }
                     }
                 }
-                const uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+                const uint32_t w0[4] = {wv[0][u].x, wv[0][u].y, wv[0][u].z, wv[0][u].w};
+                const uint32_t w1[4] = {wv[NR - 1][u].x, wv[NR - 1][u].y, wv[NR - 1][u].z,
+                                        wv[NR - 1][u].w};
 #pragma unroll
                 for (int s = 0; s < NS; ++s) {
-                    uint32_t b0, b1;
+                    // the 16 bytes of row g (and g + 8) are the lane's fragment:
+                    // words (2s, 2s+1), or int8 word s widened in two halves
+                    uint32_t lo0, hi0, lo1, hi1;
                     if constexpr (INT8) {
-                        b0 = i8x2_to_bf16x2(ww[s], 0);
-                        b1 = i8x2_to_bf16x2(ww[s], 2);
+                        lo0 = i8x2_to_bf16x2(w0[s], 0);
+                        hi0 = i8x2_to_bf16x2(w0[s], 2);
+                        lo1 = WA ? i8x2_to_bf16x2(w1[s], 0) : 0u;
+                        hi1 = WA ? i8x2_to_bf16x2(w1[s], 2) : 0u;
                     } else {
-                        b0 = ww[2 * s];
-                        b1 = ww[2 * s + 1];
+                        lo0 = w0[2 * s];
+                        hi0 = w0[2 * s + 1];
+                        lo1 = w1[2 * s];
+                        hi1 = w1[2 * s + 1];
                     }
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
-                        mma_bf16_16816(acc[mt], xa[mt][2 * s], xb[mt][2 * s], xa[mt][2 * s + 1],
-                                 xb[mt][2 * s + 1], b0, b1);
+                    for (int mt = 0; mt < MT; ++mt) {
+                        if constexpr (WA)
+                            mma_bf16_16816(acc[mt], lo0, lo1, hi0, hi1, xa[mt][2 * s],
+                                           xa[mt][2 * s + 1]);
+                        else
+                            mma_bf16_16816(acc[mt], xa[mt][2 * s], xb[mt][2 * s],
+                                           xa[mt][2 * s + 1], xb[mt][2 * s + 1], lo0, hi0);
+                    }
                 }
             }
         }
@@ -181,48 +242,44 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
                 d[r] = t;
             }
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int m = m0 + mt * 16 + g + 8 * half;
-                if (m >= a.M) continue;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int row = row0 + 2 * q + j;
-                    if (row >= a.N) continue;
-                    float v = d[2 * half + j];
-                    if constexpr (INT8) v *= bf2f(a.scale[row]);
-                    if (a.bias) v += bf2f(a.bias[row]);
-                    const size_t o = (size_t)m * a.N + row;
-                    if constexpr (EPI == EPI_STORE) {
-                        a.out[o] = f2bf(v);
-                    } else if constexpr (EPI == EPI_GELU) {
-                        a.out[o] = f2bf(gelu_tanh(v));
-                    } else if constexpr (EPI == EPI_RESID) {
-                        a.out[o] = f2bf(bf2f(a.out[o]) + v);
-                    } else if constexpr (EPI == EPI_RESID32) {
-                        a.out32[o] += v;
-                    } else if constexpr (EPI == EPI_QKV) {
-                        const int dh = a.head_dim;
-                        const int hj = row / (3 * dh);
-                        const int cidx = (row / dh) % 3;
-                        const int e = row % dh;
-                        if (cidx == 0) {
-                            a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e] = f2bf(v);
-                        } else {
-                            int seq, slot;
-                            if (a.T > 0) { seq = m / a.T; slot = m - seq * a.T; }
-                            else { seq = m; slot = *a.len_ptr; }
-                            if (slot >= 0 && slot < a.max_seq) {
-                                uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
-                                cache[(((size_t)seq * a.n_head + hj) * a.max_seq + slot) * dh + e] =
-                                    f2bf(v);
-                            } else if (a.err) {
-                                atomicOr(a.err, kErrSlot);
-                            }
+            for (int e = 0; e < 4; ++e) {
+                int m, row;
+                tile_elem<WA>(e, mt, m0, row0, g, q, m, row);
+                if (m >= a.M || row >= a.N) continue;
+                float v = d[e];
+                if constexpr (INT8) v *= bf2f(a.scale[row]);
+                if (a.bias) v += bf2f(a.bias[row]);
+                const size_t o = (size_t)m * a.N + row;
+                if constexpr (EPI == EPI_STORE) {
+                    a.out[o] = f2bf(v);
+                } else if constexpr (EPI == EPI_GELU) {
+                    a.out[o] = f2bf(gelu_tanh(v));
+                } else if constexpr (EPI == EPI_RESID) {
+                    a.out[o] = f2bf(bf2f(a.out[o]) + v);
+                } else if constexpr (EPI == EPI_RESID32) {
+                    a.out32[o] += v;
+                } else if constexpr (EPI == EPI_QKV) {
+                    const int dh = a.head_dim;
+                    const int hj = row / (3 * dh);
+                    const int cidx = (row / dh) % 3;
+                    const int e2 = row % dh;
+                    if (cidx == 0) {
+                        a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e2] = f2bf(v);
+                    } else {
+                        int seq, slot;
+                        if (a.T > 0) { seq = m / a.T; slot = m - seq * a.T; }
+                        else { seq = m; slot = *a.len_ptr; }
+                        if (slot >= 0 && slot < a.max_seq) {
+                            uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
+                            cache[(((size_t)seq * a.n_head + hj) * a.max_seq + slot) * dh + e2] =
+                                f2bf(v);
+                        } else if (a.err) {
+                            atomicOr(a.err, kErrSlot);
                         }
-                    } else if constexpr (EPI == EPI_ARGMAX) {
-                        if (a.logits) a.logits[o] = v;
-                        atomicMax(&s_best[m], pack_argmax(v, (uint32_t)row));
                     }
+                } else if constexpr (EPI == EPI_ARGMAX) {
+                    if (a.logits) a.logits[o] = v;
+                    atomicMax(&s_best[m], pack_argmax(v, (uint32_t)row));
                 }
             }
         }
@@ -255,7 +312,7 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
     }
 }
 
-template <int MT, bool INT8, int EPI, bool LNF>
+template <int MT, bool INT8, int EPI, bool LNF, bool WA>
 static int occupancy(size_t smem) {
     // cached per instance and dynamic shared-memory size (a few sizes per model)
     static size_t keys[8];
@@ -264,7 +321,7 @@ static int occupancy(size_t smem) {
     for (int i = 0; i < n; ++i)
         if (keys[i] == smem) return vals[i];
     int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, linear_kernel<MT, INT8, EPI, LNF>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, linear_kernel<MT, INT8, EPI, LNF, WA>,
                                                       kLinThreads, smem) != cudaSuccess || o < 1)
         o = 1;
     if (n < 8) {
@@ -275,29 +332,46 @@ static int occupancy(size_t smem) {
     return o;
 }
 
-template <int MT, bool INT8, int EPI, bool LNF>
+template <int MT, bool INT8, int EPI, bool LNF, bool WA>
 static cudaError_t launch_t(const LinearArgs &a, int num_sms, cudaStream_t s) {
+    constexpr int RG = WA ? 16 : 8, TT = WA ? 8 * MT : 16 * MT;
     const size_t smem = LNF ? (size_t)a.M * (a.K * 2 + 64) : 0;
-    const long long tasks = (long long)((a.N + 7) / 8) * ((a.M + 16 * MT - 1) / (16 * MT));
-    const long long cap = (long long)num_sms * occupancy<MT, INT8, EPI, LNF>(smem);
+    const long long tasks = (long long)((a.N + RG - 1) / RG) * ((a.M + TT - 1) / TT);
+    const long long cap = (long long)num_sms * occupancy<MT, INT8, EPI, LNF, WA>(smem);
     // the fewest waves the SMs can hold, then just enough CTAs for that many
     const long long waves = (tasks + cap - 1) / cap;
     long long blocks = (tasks + waves - 1) / waves;
     if (blocks < 1) blocks = 1;
-    return launch_pdl_smem(linear_kernel<MT, INT8, EPI, LNF>, dim3((unsigned)blocks),
+    return launch_pdl_smem(linear_kernel<MT, INT8, EPI, LNF, WA>, dim3((unsigned)blocks),
                            dim3(kLinThreads), smem, s, a);
 }
 
-template <int MT, bool INT8, bool LNF>
+// Weights as the A operand (16-row tasks, MTA token tiles of 8) when those
+// tasks fill at least one wave of the SMs: half the mma steps and half the
+// activation fragments per weight byte, two rows' loads in flight per lane.
+// Fewer, larger tasks lose when they leave SMs idle (4096-row matrices), so
+// those keep the B-operand form (8-row tasks, MTB token tiles of 16); so do
+// more than 32 tokens (MTA = 0).
+template <int MTA, int MTB, bool INT8, int EPI, bool LNF>
+static cudaError_t launch_o(const LinearArgs &a, int num_sms, cudaStream_t s) {
+    if constexpr (MTA > 0) {
+        const size_t smem = LNF ? (size_t)a.M * (a.K * 2 + 64) : 0;
+        const long long cap = (long long)num_sms * occupancy<MTA, INT8, EPI, LNF, true>(smem);
+        if ((a.N + 15) / 16 >= cap) return launch_t<MTA, INT8, EPI, LNF, true>(a, num_sms, s);
+    }
+    return launch_t<MTB, INT8, EPI, LNF, false>(a, num_sms, s);
+}
+
+template <int MTA, int MTB, bool INT8, bool LNF>
 static cudaError_t launch_epi(const LinearArgs &a, int num_sms, cudaStream_t s) {
     switch (a.epi) {
-        case EPI_STORE: return launch_t<MT, INT8, EPI_STORE, LNF>(a, num_sms, s);
-        case EPI_GELU: return launch_t<MT, INT8, EPI_GELU, LNF>(a, num_sms, s);
-        case EPI_RESID: return launch_t<MT, INT8, EPI_RESID, LNF>(a, num_sms, s);
-        case EPI_RESID32: return launch_t<MT, INT8, EPI_RESID32, LNF>(a, num_sms, s);
-        case EPI_QKV: return launch_t<MT, INT8, EPI_QKV, LNF>(a, num_sms, s);
+        case EPI_STORE: return launch_o<MTA, MTB, INT8, EPI_STORE, LNF>(a, num_sms, s);
+        case EPI_GELU: return launch_o<MTA, MTB, INT8, EPI_GELU, LNF>(a, num_sms, s);
+        case EPI_RESID: return launch_o<MTA, MTB, INT8, EPI_RESID, LNF>(a, num_sms, s);
+        case EPI_RESID32: return launch_o<MTA, MTB, INT8, EPI_RESID32, LNF>(a, num_sms, s);
+        case EPI_QKV: return launch_o<MTA, MTB, INT8, EPI_QKV, LNF>(a, num_sms, s);
         case EPI_ARGMAX:
-            if constexpr (!INT8) return launch_t<MT, false, EPI_ARGMAX, LNF>(a, num_sms, s);
+            if constexpr (!INT8) return launch_o<MTA, MTB, false, EPI_ARGMAX, LNF>(a, num_sms, s);
             return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
@@ -305,19 +379,26 @@ static cudaError_t launch_epi(const LinearArgs &a, int num_sms, cudaStream_t s) 
 
 template <bool INT8, bool LNF>
 static cudaError_t launch_mt(const LinearArgs &a, int num_sms, cudaStream_t s) {
-    if (a.M <= 16) return launch_epi<1, INT8, LNF>(a, num_sms, s);
-    if (a.M <= 32) return launch_epi<2, INT8, LNF>(a, num_sms, s);
-    return launch_epi<4, INT8, LNF>(a, num_sms, s);
+    if (a.M <= 8) return launch_epi<1, 1, INT8, LNF>(a, num_sms, s);
+    if (a.M <= 16) return launch_epi<2, 1, INT8, LNF>(a, num_sms, s);
+    if (a.M <= 32) return launch_epi<4, 2, INT8, LNF>(a, num_sms, s);
+    return launch_epi<0, 4, INT8, LNF>(a, num_sms, s);
+}
+
+template <bool INT8, int EPI, bool WA>
+static cudaError_t prepare_mt_o() {
+    occupancy<1, INT8, EPI, false, WA>(0);
+    occupancy<2, INT8, EPI, false, WA>(0);
+    occupancy<4, INT8, EPI, false, WA>(0);
+    // only the fused-LayerNorm instance (one token tile) uses dynamic shared memory
+    return cudaFuncSetAttribute(linear_kernel<1, INT8, EPI, true, WA>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kLnFuseSmemMax);
 }
 
 template <bool INT8, int EPI>
 static cudaError_t prepare_mt() {
-    occupancy<1, INT8, EPI, false>(0);
-    occupancy<2, INT8, EPI, false>(0);
-    occupancy<4, INT8, EPI, false>(0);
-    // only the fused-LayerNorm instance (one token tile) uses dynamic shared memory
-    return cudaFuncSetAttribute(linear_kernel<1, INT8, EPI, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kLnFuseSmemMax);
+    const cudaError_t e = prepare_mt_o<INT8, EPI, false>();
+    return e ? e : prepare_mt_o<INT8, EPI, true>();
 }
 
 // Occupancies and shared-memory limits of every instance, outside any capture.
@@ -347,8 +428,8 @@ cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s) {
     if (a.epi == EPI_ARGMAX && (a.int8 || a.M > kMaxBatch)) return cudaErrorInvalidValue;
     if (a.ln_x) {
         if (!linear_can_fuse_ln(a)) return cudaErrorInvalidValue;
-        return a.int8 ? launch_epi<1, true, true>(a, num_sms, s)
-                      : launch_epi<1, false, true>(a, num_sms, s);
+        return a.int8 ? launch_epi<1, 1, true, true>(a, num_sms, s)
+                      : launch_epi<1, 1, false, true>(a, num_sms, s);
     }
     return a.int8 ? launch_mt<true, false>(a, num_sms, s) : launch_mt<false, false>(a, num_sms, s);
 }

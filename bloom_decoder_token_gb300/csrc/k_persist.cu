@@ -55,23 +55,6 @@ constexpr long long kPWaitCycles = 4000000000ll;
 
 static_assert(kLnThreads == kPThreads, "LayerNorm rows are normalised by one whole block");
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     (uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Activations written by other blocks of this launch: coherent (L1-cached,
 // invalidated by the barrier's acquire fence), never ld.global.nc.
 __device__ __forceinline__ uint4 ld_coherent(const void *p) {

@@ -19,17 +19,25 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two int8 codes (bytes i, i+1 of w) -> bf16x2, exactly: 2^23 + (q + 128) is an
-// exact float whose low mantissa byte is q + 128; subtracting 2^23 + 128 leaves q,
-// and |q| <= 128 is exact in bf16.
+// Two int8 codes (bytes i, i+1 of w) -> bf16x2, exactly.  With the sign bits
+// flipped (w ^ 0x80808080), byte permutes place q + 128 as the low mantissa
+// byte of two floats 2^23 + (q + 128); one paired float32 add removes
+// 2^23 + 128 from both and one conversion packs them (|q| <= 128 is exact in
+// bf16).  Four instructions per pair, the flip shared by a word's two pairs.
 __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int i) {
-    const uint32_t b0 = ((w >> (8 * i)) & 0xffu) ^ 0x80u;
-    const uint32_t b1 = ((w >> (8 * i + 8)) & 0xffu) ^ 0x80u;
-    const float f0 = __uint_as_float(0x4b000000u | b0) - 8388736.0f;
-    const float f1 = __uint_as_float(0x4b000000u | b1) - 8388736.0f;
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f1), "f"(f0));
-    return r;
+    const uint32_t wx = w ^ 0x80808080u;
+    uint32_t u0, u1;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(u0) : "r"(wx), "r"(0x4b000000u), "r"(0x7540u | i));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(u1) : "r"(wx), "r"(0x4b000000u), "r"(0x7540u | (i + 1)));
+    const unsigned long long p = ((unsigned long long)u1 << 32) | u0;
+    const unsigned long long off = 0xcb000080cb000080ull;   // -(2^23 + 128) in both halves
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(p), "l"(off));
+    uint32_t o;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(o)
+        : "f"(__uint_as_float((uint32_t)(r >> 32))), "f"(__uint_as_float((uint32_t)r)));
+    return o;
 }
 
 // Epilogue of one 16x8 accumulator tile (token rows m_base + g, m_base + g + 8;

@@ -48,9 +48,11 @@ def test_layernorm_constant_row_gives_beta():
 
 
 # ---------------------------------------------------------------- linear
+# The last four take the A-operand form (16-row tasks, at least a wave of them
+# on 152 SMs) with 1, 2 and 4 token tiles, ragged rows and a ragged K tail.
 SHAPES = [(1, 3072, 1024), (3, 100, 64), (8, 4096, 4096), (5, 13, 16384), (16, 1000, 1024),
           (33, 50, 512), (2, 4097, 256), (8, 257, 14336), (64, 600, 1040), (1, 40, 57344),
-          (24, 1, 4096), (1, 12288, 4096)]
+          (24, 1, 4096), (1, 12288, 4096), (3, 16000, 208), (13, 8200, 512), (24, 12300, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -84,6 +86,25 @@ def test_linear(M, N, K, int8, epi):
     else:
         ref = f64(y0) + acc
     assert_kernel_close(y, ref, what=f"linear {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("N", [256, 8192], ids=["b_operand", "a_operand"])
+def test_linear_int8_every_code(N):
+    """Every int8 code, -128 included, at byte positions inside a lane's 16-byte
+    fragment, across lanes and across chunks, is widened exactly: with unit
+    scales, no bias and one-hot activations y[m][n] = q[n][p_m]."""
+    K = 256
+    n = torch.arange(N).unsqueeze(1)
+    k = torch.arange(K).unsqueeze(0)
+    q = ((n + k) % 256).to(torch.uint8).view(torch.int8)
+    pos = [0, 1, 2, 3, 13, 31, 70, 255]
+    x = torch.zeros(len(pos), K, dtype=torch.bfloat16)
+    for m, p in enumerate(pos):
+        x[m, p] = 1.0
+    scale = torch.ones(N, dtype=torch.bfloat16)
+    y = bg.op_linear(x.to(DEV), q=q.to(DEV), scale=scale.to(DEV))
+    expect = torch.stack([q[:, p].float() for p in pos])
+    assert torch.equal(y.cpu().float(), expect)
 
 
 def test_linear_zero_bias_and_empty_batch():
