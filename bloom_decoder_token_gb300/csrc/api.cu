@@ -137,6 +137,15 @@ struct bloom_model {
     bool tcd = false;
     TcMap head_wmap;
     TcMap head_xmaps[kTcNtClasses];
+    // the bf16 block linears of decode steps of >= kTcDecodeBlockMinM sequences on
+    // the tensor cores: weight maps [layer][TC_*] (box 128 rows), activation maps
+    // [TC_X_*][token-column class], split-K partial tiles and tickets
+    bool tcb = false;
+    std::vector<TcMap> dwmaps;
+    TcMap dxmaps[3][kTcNtClasses];
+    void *dscratch = nullptr;
+    float *dpart = nullptr;
+    int *dticket = nullptr;
     // persistent decode step: grid (0 = not available), barrier words, phase tables
     int pgrid = 0;
     int pmax_phases = 0;
@@ -197,6 +206,7 @@ extern "C" bloom_status bloom_destroy(bloom_model *m) {
     for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
     for (auto &p : m->plans) cudaFree(p.phases);
     if (m->pscratch) cudaFree(m->pscratch);
+    if (m->dscratch) cudaFree(m->dscratch);
     if (m->cap) cudaStreamDestroy(m->cap);
     if (m->ws) cudaFree(m->ws);
     delete m;
@@ -306,6 +316,45 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
             st2 = fail(BLOOM_E_CUDA, "LM head setup: %s", cudaGetErrorString(cudaGetLastError()));
         else
             m->tcd = true;
+    }
+    if (!st2 && m->tcd && !i8 && cfg->max_batch >= kTcDecodeBlockMinM) {
+        const int F = cfg->ffn;
+        const int ntmax = gemv_tc_nt(cfg->max_batch);
+        bool ok = true;
+        m->dwmaps.resize((size_t)cfg->n_layer * TC_PER_LAYER);
+        const int bw = gemv_tc_box_rows_w();
+        for (int l = 0; ok && l < cfg->n_layer; ++l) {
+            const bloom_layer_weights &L = w->layers[l];
+            TcMap *wm = &m->dwmaps[(size_t)l * TC_PER_LAYER];
+            ok = gemm_make_map(wm[TC_QKV].b, L.qkv.w, 3 * h, h, bw) &&
+                 gemm_make_map(wm[TC_O].b, L.o.w, h, h, bw) &&
+                 gemm_make_map(wm[TC_UP].b, L.up.w, F, h, bw) &&
+                 gemm_make_map(wm[TC_DOWN].b, L.down.w, h, F, bw);
+        }
+        for (int ci = 0; ok && ci < kTcNtClasses && (16 << ci) <= ntmax; ++ci)
+            ok = gemm_make_map(m->dxmaps[TC_X_A][ci].b, m->a, cfg->max_batch, h, 16 << ci) &&
+                 gemm_make_map(m->dxmaps[TC_X_O][ci].b, m->o, cfg->max_batch, h, 16 << ci) &&
+                 gemm_make_map(m->dxmaps[TC_X_U][ci].b, m->u, cfg->max_batch, F, 16 << ci);
+        // split-K scratch for the largest of the four shapes
+        const int shapes[4][2] = {{3 * h, h}, {h, h}, {F, h}, {h, F}};
+        size_t pf = 0;
+        int tk = 0;
+        for (const auto &sh : shapes) {
+            pf = std::max(pf, gemv_tc_part_floats(sh[0], sh[1], cfg->max_batch, m->num_sms));
+            tk = std::max(tk, (sh[0] + 127) / 128);
+        }
+        const size_t pb = align256(pf * 4);
+        const size_t bytes = pb + (size_t)tk * 4;
+        if (!ok) {
+            st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the decode linears could not be encoded");
+        } else if (cudaMalloc(&m->dscratch, bytes) != cudaSuccess ||
+                   cudaMemset(m->dscratch, 0, bytes) != cudaSuccess) {
+            st2 = fail(BLOOM_E_OOM, "decode-linear scratch of %zu bytes", bytes);
+        } else {
+            m->dpart = (float *)m->dscratch;
+            m->dticket = (int *)((char *)m->dscratch + pb);
+            m->tcb = true;
+        }
     }
     if (!st2 && (cfg->flags & BLOOM_FLAG_PERSISTENT)) {
         m->pgrid = persist_grid(i8);   // 0: no cooperative launch of one block per SM here
@@ -441,17 +490,36 @@ static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t
     return launch_gemv_tc(m->head_wmap.b, m->head_xmaps[ci].b, g, nt, s);
 }
 
+// A decode block linear on the tensor-core decode kernel: bf16 weights, at least
+// kTcDecodeBlockMinM sequences, and a matrix that is wide (>= 8192 rows) or long
+// (K >= 8192), or at least 64 sequences.  Measured per kernel on GB300 (7b1
+// shapes, back-to-back launches): at 16-64 tokens it beats the weight-streaming
+// kernel on the QKV, up and down matrices (32 tokens: 23 / 26 / 43 us vs
+// 33 / 49 / 48 us), not on the 4096 x 4096 dense one below 64 tokens.
+static bool use_tc_linear(const bloom_model *m, const LinearArgs &a) {
+    return m->tcb && a.T == 0 && !a.int8 && !a.ln_x && a.M >= kTcDecodeBlockMinM &&
+           a.M <= m->cfg.max_batch && (a.N >= 8192 || a.K >= 8192 || a.M >= 64);
+}
+
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
-// kTcMinM tokens or more, else the weight-streaming kernel.  Decode block
-// linears stay on the weight-streaming kernel at every batch: measured in whole
-// decode steps, its small shared-memory footprint lets the next kernel's CTAs
-// start under the previous one's tail (programmatic dependent launch), which
-// outweighs the tensor-core kernel's faster stream on 2-134 MB matrices (the
-// tensor-core decode linear serves the LM head, enqueue_head).
+// kTcMinM tokens or more, the tensor-core decode kernel where use_tc_linear
+// says so, else the weight-streaming kernel.
 static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wmap, int xmap,
                               cudaStream_t s) {
     if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x)
         return launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
+    if (use_tc_linear(m, a)) {
+        const int nt = gemv_tc_nt(a.M);
+        int ci = 0;
+        while ((16 << ci) < nt) ++ci;
+        GemvTcArgs g;
+        g.a = a;
+        g.splits = gemv_tc_splits(a.N, a.K, m->num_sms, a.epi);
+        g.part = m->dpart;
+        g.ticket = m->dticket;
+        return launch_gemv_tc(m->dwmaps[(size_t)l * TC_PER_LAYER + wmap].b, m->dxmaps[xmap][ci].b,
+                              g, nt, s);
+    }
     return launch_linear(a, m->num_sms, s);
 }
 

@@ -22,8 +22,8 @@
 // In the decode step this kernel runs the tied LM head (the largest single
 // weight stream: V x h) for 8 or more sequences, where it streams at twice the
 // weight-streaming kernel's rate (2 GB head of the 7b1 shape, 32 sequences:
-// 334 us vs 675 us); the block linears stay on the weight-streaming kernel,
-// whose small shared-memory footprint lets successive kernels overlap.
+// 334 us vs 675 us), and the bf16 block linears from 16 sequences on where
+// they are wide or long (7b1 shape, 32 sequences: up 26 us vs 49 us).
 // Narrow matrices split K over several CTAs so that the grid fills the GPU;
 // each split stores its float32 partial tile and the last split of a row tile
 // to finish (a ticket, no waiting) sums the partials in split order, so the
@@ -42,6 +42,7 @@ constexpr int kGvBK = 64;                         // k per stage: one 128-byte s
 constexpr int kGvThreads = 192;                   // 6 warps
 constexpr int kGvWBytes = kGvRows * kGvBK * 2;    // 16 KB
 constexpr int kGvSmemBudget = 108 * 1024;         // two CTAs per SM
+constexpr int kGvTargetCtas = 120;                // CTAs a K split aims for
 
 template <int NT>
 struct GvCfg {
@@ -296,23 +297,20 @@ int gemv_tc_nt(int M) {
 
 // K splits per row tile: the fewest that fill the GPU's CTA slots (two CTAs
 // per SM) in whole waves, at most one split per 4 k-blocks.
+// K splits of a launch: enough CTAs for about kGvTargetCtas SMs and no more.
+// Measured on GB300 at 16-64 tokens, an unsplit 96- or 128-tile matrix streams
+// at 65-79 % of the copy peak while 2-7 splits of it (more CTAs, each partial
+// tile written, and summed by the last split) ran at 27-55 %; a 32-tile matrix
+// wants 4.
 int gemv_tc_splits(int N, int K, int num_sms, int epi) {
+    (void)num_sms;
     if (epi == EPI_ARGMAX) return 1;
     const int tiles = (N + kGvRows - 1) / kGvRows;
     const int nkb = (K + kGvBK - 1) / kGvBK;
-    const int slots = 2 * num_sms;
-    int best = 1;
-    double best_eff = 0.0;
-    for (int s = 1; s <= 16 && s * 4 <= nkb; ++s) {
-        const long long ctas = (long long)tiles * s;
-        const long long waves = (ctas + slots - 1) / slots;
-        const double eff = (double)ctas / (double)(waves * slots);
-        if (eff > best_eff + 0.05) {
-            best_eff = eff;
-            best = s;
-        }
-    }
-    return best;
+    int s = (kGvTargetCtas + tiles / 2) / tiles;   // rounded: 96 or 128 tiles -> 1, 32 -> 4
+    if (s > 16) s = 16;
+    while (s > 1 && s * 4 > nkb) --s;   // at least 4 k-blocks per split
+    return s < 1 ? 1 : s;
 }
 
 size_t gemv_tc_part_floats(int N, int K, int M, int num_sms) {

@@ -186,3 +186,16 @@ def test_decode_generation_batch16(flags):
     shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=5000, batch=16)
     w = synth.make_weights(shape, seed=12, random_affine=True)
     generate_parity(shape, w, steps=4, tol=2e-2, flags=flags)
+
+
+@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_TC_GEMM], ids=["tcgen05", "streaming"])
+def test_decode_block_linears_through_tcgen05(B, flags):
+    """An 8192-wide MLP (up: N = 8192, down: K = 8192) at 16 and 32 sequences:
+    the decode step runs those two linears on the tensor-core decode kernel
+    (down with its K split summed by the last split), against the oracle, and
+    against the weight-streaming path for the same inputs."""
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=4096, ffn=8192, batch=B, prompt=8,
+                                        ragged=True)
+    w = synth.make_weights(shape, seed=21, random_affine=True)
+    generate_parity(shape, w, steps=3, tol=2e-2, flags=flags)
