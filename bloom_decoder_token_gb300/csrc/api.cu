@@ -493,9 +493,10 @@ static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t
 // A decode block linear on the tensor-core decode kernel: bf16 weights, at least
 // kTcDecodeBlockMinM sequences, and a matrix that is wide (>= 8192 rows) or long
 // (K >= 8192), or at least 64 sequences.  Measured per kernel on GB300 (7b1
-// shapes, back-to-back launches): at 16-64 tokens it beats the weight-streaming
+// shapes, back-to-back launches): at 8-64 tokens it beats the weight-streaming
 // kernel on the QKV, up and down matrices (32 tokens: 23 / 26 / 43 us vs
-// 33 / 49 / 48 us), not on the 4096 x 4096 dense one below 64 tokens.
+// 33 / 49 / 48 us; 8 and 16 tokens share its 16-column tile: 21 / 25 / 33 us
+// vs 22 / 31 / 35 us at 8), not on the 4096 x 4096 dense one below 64 tokens.
 static bool use_tc_linear(const bloom_model *m, const LinearArgs &a) {
     return m->tcb && a.T == 0 && !a.int8 && !a.ln_x && a.M >= kTcDecodeBlockMinM &&
            a.M <= m->cfg.max_batch && (a.N >= 8192 || a.K >= 8192 || a.M >= 64);

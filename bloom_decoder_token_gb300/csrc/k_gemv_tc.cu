@@ -22,7 +22,7 @@
 // In the decode step this kernel runs the tied LM head (the largest single
 // weight stream: V x h) for 8 or more sequences, where it streams at twice the
 // weight-streaming kernel's rate (2 GB head of the 7b1 shape, 32 sequences:
-// 334 us vs 675 us), and the bf16 block linears from 16 sequences on where
+// 334 us vs 675 us), and the bf16 block linears from 8 sequences on where
 // they are wide or long (7b1 shape, 32 sequences: up 26 us vs 49 us).
 // Narrow matrices split K over several CTAs so that the grid fills the GPU;
 // each split stores its float32 partial tile and the last split of a row tile

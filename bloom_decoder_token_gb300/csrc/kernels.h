@@ -122,7 +122,7 @@ struct GemvTcArgs {
     int *ticket = nullptr;
 };
 constexpr int kTcDecodeMinM = 8;    // decode steps of at least this many sequences: LM head on it
-constexpr int kTcDecodeBlockMinM = 16;   // ... and, from this many, the wide or long block linears
+constexpr int kTcDecodeBlockMinM = 8;    // ... and the wide or long block linears
 int gemv_tc_nt(int M);
 int gemv_tc_splits(int N, int K, int num_sms, int epi);
 size_t gemv_tc_part_floats(int N, int K, int M, int num_sms);

@@ -65,7 +65,8 @@ enum {
                                     the decode linear kernel that consumes it */
     BLOOM_FLAG_NO_TC_GEMM = 8,   /* every linear on the weight-streaming kernel instead of the
                                     tensor-core (tcgen05) kernels: the prefill GEMM (>= 128
-                                    tokens) and the decode LM head (>= 8 sequences) */
+                                    tokens), the decode LM head (>= 8 sequences) and the wide
+                                    or long bf16 decode block linears (>= 8 sequences) */
     BLOOM_FLAG_PERSISTENT = 16   /* decode steps of <= 16 sequences as one persistent
                                     cooperative launch (all layers as phases separated by grid
                                     barriers) instead of one launch per operation replayed as a

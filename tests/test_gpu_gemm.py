@@ -188,10 +188,10 @@ def test_decode_generation_batch16(flags):
     generate_parity(shape, w, steps=4, tol=2e-2, flags=flags)
 
 
-@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("B", [8, 16, 32])
 @pytest.mark.parametrize("flags", [0, bg.FLAG_NO_TC_GEMM], ids=["tcgen05", "streaming"])
 def test_decode_block_linears_through_tcgen05(B, flags):
-    """An 8192-wide MLP (up: N = 8192, down: K = 8192) at 16 and 32 sequences:
+    """An 8192-wide MLP (up: N = 8192, down: K = 8192) at 8, 16 and 32 sequences:
     the decode step runs those two linears on the tensor-core decode kernel
     (down with its K split summed by the last split), against the oracle, and
     against the weight-streaming path for the same inputs."""
