@@ -524,17 +524,26 @@ static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wm
     return launch_linear(a, m->num_sms, s);
 }
 
-// The LayerNorm feeding a linear layer: fused into the persistent kernel's
-// prologue when it applies (decode, shared memory permitting), else one
-// LayerNorm launch writing the bf16 activations the linear layer reads.
+// Whether the LayerNorm feeding linear `a` runs inside it: allowed by the flags
+// and the linear kernel, and `a` does not run on a tensor-core kernel (those
+// read their activations from global memory through a TMA map).
+static bool ln_fuses(const bloom_model *m, const LinearArgs &a) {
+    return !(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION) && linear_can_fuse_ln(a) &&
+           !use_tc_head(m, a) && !use_tc_linear(m, a);
+}
+
+// The LayerNorm feeding a linear layer: fused into the linear kernel's prologue
+// when ln_fuses says so, else one LayerNorm launch writing the bf16 activations
+// the linear layer reads.
 static cudaError_t fused_ln(bloom_model *m, LinearArgs &a, const float *x, const void *g,
                             const void *b, cudaStream_t s) {
-    a.ln_x = x;
-    a.ln_g = (const uint16_t *)g;
-    a.ln_b = (const uint16_t *)b;
-    a.ln_eps = m->cfg.ln_eps;
-    if (!(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION) && linear_can_fuse_ln(a)) return cudaSuccess;
-    a.ln_x = nullptr;
+    if (ln_fuses(m, a)) {
+        a.ln_x = x;
+        a.ln_g = (const uint16_t *)g;
+        a.ln_b = (const uint16_t *)b;
+        a.ln_eps = m->cfg.ln_eps;
+        return cudaSuccess;
+    }
     return launch_layernorm_f32(x, (const uint16_t *)g, (const uint16_t *)b, a.M, a.K,
                                 m->cfg.ln_eps, const_cast<uint16_t *>(a.x), 1, nullptr, s);
 }
@@ -666,18 +675,15 @@ extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
     if (!m) return 0;
     if (use_persistent(m, batch)) return 1;
     // embedding; per layer LN1, QKV, attention, dense, LN2, up, down; ln_f, head --
-    // less the LayerNorm launches that the linear kernels absorb
-    const bool fusable = !(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION);
-    LinearArgs t;
-    t.M = batch;
-    t.K = m->cfg.hidden;
-    t.int8 = m->cfg.weight_dtype == BLOOM_WEIGHT_INT8;
-    t.epi = EPI_QKV;
-    const int block_ln = (fusable && linear_can_fuse_ln(t)) ? 0 : 2;
-    t.int8 = 0;
-    t.epi = EPI_ARGMAX;
-    const int head_ln = (fusable && linear_can_fuse_ln(t)) ? 0 : 1;
-    return 1 + (5 + block_ln) * m->cfg.n_layer + 1 + head_ln;
+    // less the LayerNorm launches that the linear kernels absorb (ln_fuses)
+    const bloom_config &c = m->cfg;
+    const int i8 = c.weight_dtype == BLOOM_WEIGHT_INT8;
+    LinearArgs qkv = lin_args(bloom_linear{}, i8, m->a, batch, 3 * c.hidden, c.hidden, EPI_QKV);
+    LinearArgs up = lin_args(bloom_linear{}, i8, m->a, batch, c.ffn, c.hidden, EPI_GELU);
+    LinearArgs head = lin_args(bloom_linear{}, 0, m->xl, batch, c.vocab, c.hidden, EPI_ARGMAX);
+    const int block_ln = (ln_fuses(m, qkv) ? 0 : 1) + (ln_fuses(m, up) ? 0 : 1);
+    const int head_ln = ln_fuses(m, head) ? 0 : 1;
+    return 1 + (5 + block_ln) * c.n_layer + 1 + head_ln;
 }
 
 // Key ranges per (sequence, head) in the persistent step: one visit of every
