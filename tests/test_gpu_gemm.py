@@ -199,3 +199,14 @@ def test_decode_block_linears_through_tcgen05(B, flags):
                                         ragged=True)
     w = synth.make_weights(shape, seed=21, random_affine=True)
     generate_parity(shape, w, steps=3, tol=2e-2, flags=flags)
+
+
+def test_decode_qkv_through_tcgen05():
+    """A 2816-wide stack with 22 heads of 128 at 8 sequences: the decode QKV
+    linear (8448 rows) runs on the tensor-core decode kernel with its K split in
+    two, the Q/K/V scatter into the cache applied by the last split; up (11264
+    rows) unsplit; down (K = 11264) split five ways.  Against the oracle."""
+    shape = synth.PRESETS["560m"].with_(n_layer=1, hidden=2816, n_head=22, ffn=11264,
+                                        vocab=4096, batch=8, prompt=8, ragged=True)
+    w = synth.make_weights(shape, seed=23, random_affine=True)
+    generate_parity(shape, w, steps=2, tol=2e-2)
