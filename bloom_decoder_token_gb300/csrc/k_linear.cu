@@ -5,19 +5,24 @@
 // read W once ("DeepSpeed Inference", III.A), so the kernel is built around one
 // coalesced pass over W with as little instruction work per byte as possible:
 //
-//  * a CTA (8 warps) owns 8 consecutive weight rows and a tile of up to 16*MT
+//  * a CTA (8 warps) owns a task of consecutive weight rows and a tile of
 //    tokens; its warps split K into interleaved chunks (lane (g, q) reads 16
-//    bytes of row g at offset 16q of the chunk, so each warp load covers 8 rows
-//    x 64 bytes), every CTA streams its rows in order with several chunks in
-//    flight per lane (output-dimension tiling plus an input-dimension split, as
-//    in SBI-GeMM, "DeepSpeed Inference", III.C.1);
-//  * the 16 bytes a lane loads ARE its mma.sync m16n8k16 B fragment: within a
+//    bytes of its row(s) at offset 16q of the chunk), every CTA streams its
+//    rows in order with several chunks in flight per lane (output-dimension
+//    tiling plus an input-dimension split, as in SBI-GeMM, "DeepSpeed
+//    Inference", III.C.1);
+//  * the 16 bytes a lane loads ARE an mma.sync m16n8k16 fragment: within a
 //    chunk, logical k positions {2q, 2q+1, 2q+8, 2q+9} of mma step s are bound
 //    to physical elements q*EPL + 4s + {0..3}.  The activations use the same
 //    binding, so the dot product is unchanged while both operands come straight
-//    from 16-byte loads (no shared-memory staging, no shuffles);
-//  * int8 codes are widened exactly to bf16 (|q| <= 127) and the row scale is
-//    applied once in the epilogue (y = s_n * sum q x);
+//    from 16-byte loads (no shared-memory staging, no shuffles).  Two forms:
+//    weights as the B operand (8-row tasks, token tiles of 16: lane g loads row
+//    g) and, for wide matrices, as the A operand (16-row tasks, token tiles of
+//    8: lane g loads rows g and g + 8), which halves the mma steps and the
+//    activation fragments per weight byte and keeps two rows' loads in flight;
+//  * int8 codes are widened exactly to bf16 (two byte permutes, a paired
+//    float32 add and a pack per pair; |q| <= 128) and the row scale is applied
+//    once in the epilogue (y = s_n * sum q x);
 //  * the 8 warps' partial tiles are summed through shared memory (a transpose
 //    through shared memory instead of a shuffle tree, cf. III.C.2), then bias,
 //    GeLU, the float32 residual add, the head-interleaved Q/K/V scatter into
