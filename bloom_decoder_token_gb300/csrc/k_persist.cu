@@ -267,8 +267,8 @@ __device__ __forceinline__ void epi_prefetch(const LinearArgs &a, int epi, int r
 }
 
 // Epilogue of one 16 x 8 accumulator tile (tokens g, g+8; rows row0 + 2q + j),
-// the persistent counterpart of tile_epilogue: same results, operands from `p`,
-// the cache slot of the step's token in `slot`.
+// the persistent counterpart of the weight-streaming kernel's epilogue: same
+// results, operands from `p`, the cache slot of the step's token in `slot`.
 template <bool INT8, int EPI>
 __device__ __forceinline__ void epi_apply(const LinearArgs &a, const float (&d)[4], int row0,
                                           int lane, const EpiPre &p, int slot,

@@ -1,6 +1,6 @@
 // Tile-level device helpers of the weight-streaming linear kernels: the
-// mma.sync fragment op, exact int8 -> bf16 widening, the fused epilogues, the
-// LayerNorm prologue into shared memory, and the argmax publication.
+// mma.sync fragment op, exact int8 -> bf16 widening, the LayerNorm prologue
+// into shared memory, and the argmax publication.
 #pragma once
 
 #include "common.cuh"
@@ -38,58 +38,6 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int i) {
         : "=r"(o)
         : "f"(__uint_as_float((uint32_t)(r >> 32))), "f"(__uint_as_float((uint32_t)r)));
     return o;
-}
-
-// Epilogue of one 16x8 accumulator tile (token rows m_base + g, m_base + g + 8;
-// weight rows row0 + 2q, row0 + 2q + 1), lane = (g, q).  Decode QKV only: the
-// K/V of token m go to slot *len_ptr of sequence m (prefill uses its own path).
-template <bool INT8, int EPI>
-__device__ __forceinline__ void tile_epilogue(const LinearArgs &a, const float (&d)[4],
-                                              int m_base, int row0, int lane,
-                                              unsigned long long *s_best) {
-    const int g = lane >> 2, q = lane & 3;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int m = m_base + g + 8 * half;
-        if (m >= a.M) continue;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int row = row0 + 2 * q + j;
-            if (row >= a.N) continue;
-            float v = d[2 * half + j];
-            if constexpr (INT8) v *= bf2f(a.scale[row]);
-            if (a.bias) v += bf2f(a.bias[row]);
-            const size_t o = (size_t)m * a.N + row;
-            if constexpr (EPI == EPI_STORE) {
-                a.out[o] = f2bf(v);
-            } else if constexpr (EPI == EPI_GELU) {
-                a.out[o] = f2bf(gelu_tanh(v));
-            } else if constexpr (EPI == EPI_RESID) {
-                a.out[o] = f2bf(bf2f(a.out[o]) + v);
-            } else if constexpr (EPI == EPI_RESID32) {
-                a.out32[o] += v;
-            } else if constexpr (EPI == EPI_QKV) {
-                const int dh = a.head_dim;
-                const int hj = row / (3 * dh);
-                const int cidx = (row / dh) % 3;
-                const int e = row % dh;
-                if (cidx == 0) {
-                    a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e] = f2bf(v);
-                } else {
-                    const int slot = *a.len_ptr;
-                    if (slot >= 0 && slot < a.max_seq) {
-                        uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
-                        cache[(((size_t)m * a.n_head + hj) * a.max_seq + slot) * dh + e] = f2bf(v);
-                    } else if (a.err) {
-                        atomicOr(a.err, kErrSlot);
-                    }
-                }
-            } else if constexpr (EPI == EPI_ARGMAX) {
-                if (a.logits) a.logits[o] = v;
-                atomicMax(&s_best[m], pack_argmax(v, (uint32_t)row));
-            }
-        }
-    }
 }
 
 // LayerNorm of the M float32 rows a.ln_x[M][K] into shared memory as bf16
