@@ -480,10 +480,16 @@ static bool use_tc_head(const bloom_model *m, const LinearArgs &a) {
            !a.ln_x;
 }
 
-static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t s) {
-    const int nt = gemv_tc_nt(a.M);
+// Index of the activation map whose box covers nt token columns (16 << index).
+static int nt_class(int nt) {
     int ci = 0;
     while ((16 << ci) < nt) ++ci;
+    return ci;
+}
+
+static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t s) {
+    const int nt = gemv_tc_nt(a.M);
+    const int ci = nt_class(nt);
     GemvTcArgs g;
     g.a = a;
     g.splits = 1;
@@ -497,9 +503,12 @@ static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t
 // kernel on the QKV, up and down matrices (32 tokens: 23 / 26 / 43 us vs
 // 33 / 49 / 48 us; 8 and 16 tokens share its 16-column tile: 21 / 25 / 33 us
 // vs 22 / 31 / 35 us at 8), not on the 4096 x 4096 dense one below 64 tokens.
+constexpr int kTcBlockWide = 8192;   // rows or K from which a block linear qualifies
+constexpr int kTcBlockAnyM = 64;     // sequences from which every block linear does
 static bool use_tc_linear(const bloom_model *m, const LinearArgs &a) {
     return m->tcb && a.T == 0 && !a.int8 && !a.ln_x && a.M >= kTcDecodeBlockMinM &&
-           a.M <= m->cfg.max_batch && (a.N >= 8192 || a.K >= 8192 || a.M >= 64);
+           a.M <= m->cfg.max_batch &&
+           (a.N >= kTcBlockWide || a.K >= kTcBlockWide || a.M >= kTcBlockAnyM);
 }
 
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
@@ -511,8 +520,7 @@ static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wm
         return launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
     if (use_tc_linear(m, a)) {
         const int nt = gemv_tc_nt(a.M);
-        int ci = 0;
-        while ((16 << ci) < nt) ++ci;
+        const int ci = nt_class(nt);
         GemvTcArgs g;
         g.a = a;
         g.splits = gemv_tc_splits(a.N, a.K, m->num_sms, a.epi);
