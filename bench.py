@@ -1,12 +1,18 @@
 """Benchmark: greedy KV-cached generation through a BLOOM decoder stack on GB300.
 
 One step = one whole generation of the workload: prefill of the B padded
-prompts, then new_tokens - 1 decode steps (graph replays), argmax fed back on
-the device.  value = tokens/s = B * new_tokens / (time per step), the pages'
-per-token cost being its inverse (wall time / (batch x tokens)).
+prompts, then new_tokens - 1 decode steps (graph replays), the argmax fed back
+on the device.  value = tokens/s = B * new_tokens / (time per step); the
+pages' per-token cost is its inverse (wall time / (batch x tokens)).
+
+The default workload is the 7b1-shaped stack (30 layers, h 4096, 32 heads,
+vocab 250880) at batch 32, prompt 16, 100 greedy tokens.  The same line also
+carries, as extra keys, the decode step at batch 1 / 8 / 64 / 128 of that
+stack, its int8 weight-only form, and the 176B-layer-shaped stack (14 layers,
+h 14336, 112 heads) at batch 1; each with its fraction of the HBM roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config 560m|7b1|7b1int8|176b14|block] [--batch B]
+                  [--config 560m|7b1|7b1int8|176b14|block] [--batch B] [--no-extras]
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 on its own GPU (sequences are independent; no collective on the data path).
@@ -31,6 +37,9 @@ from bloom_decoder_token_gb300 import synth  # noqa: E402
 METRIC = "decode ms/token & tokens/s (batch x tokens) and % of HBM roofline, 1 GB300"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2 ** 20
+DEFAULT_CONFIG = "7b1"
+DEFAULT_BATCH = {"7b1": 32, "7b1int8": 32}
+SERIES_BATCHES = (1, 8, 32, 64, 128)   # decode-step series of the 7b1 stack
 
 
 def peaks():
@@ -42,11 +51,16 @@ def peaks():
 
 
 # ------------------------------------------------------------------ byte model
+def linear_shapes(sh: synth.Shape):
+    h, F = sh.hidden, sh.ffn
+    return {"qkv": (3 * h, h), "dense": (h, h), "up": (F, h), "down": (h, F)}
+
+
 def weight_bytes(sh: synth.Shape) -> int:
     """Algorithmic bytes of all weights one decode step reads once."""
-    h, F, V, L = sh.hidden, sh.ffn, sh.vocab, sh.n_layer
+    h, V, L = sh.hidden, sh.vocab, sh.n_layer
     per = 0
-    for N, K in [(3 * h, h), (h, h), (F, h), (h, F)]:
+    for N, K in linear_shapes(sh).values():
         per += N * K * (1 if sh.int8 else 2) + N * 2 + (N * 2 if sh.int8 else 0)   # W, bias, scales
     per += 4 * h * 2                                                               # 2 LayerNorms
     return L * per + V * h * 2 + 4 * h * 2                                         # + head E, ln_f, emb LN
@@ -60,85 +74,61 @@ def decode_step_bytes(sh: synth.Shape, B: int, keys: int) -> int:
     return weight_bytes(sh) + kv_read + kv_write + B * h * 2 + B * L * keys * 4
 
 
-def head_launch_bytes(sh: synth.Shape, B: int) -> int:
-    return sh.vocab * sh.hidden * 2 + B * sh.hidden * 2 + B * 4
+def op_bytes(sh: synth.Shape, B: int, op: str, keys: int) -> int:
+    """Algorithmic bytes of one launch of a decode-step operation: weights,
+    biases and scales once, activations read and written, cache traffic."""
+    h, F, V = sh.hidden, sh.ffn, sh.vocab
+    wb = 1 if sh.int8 else 2
+    if op in ("qkv", "dense", "up", "down"):
+        N, K = linear_shapes(sh)[op]
+        w = N * K * wb + N * 2 + (N * 2 if sh.int8 else 0)
+        act_in = B * K * 2
+        act_out = B * N * 8 if op in ("dense", "down") else B * N * 2   # float32 residual r+w
+        return w + act_in + act_out
+    if op == "attn":
+        return B * 2 * keys * h * 2 + B * keys * 4 + 2 * B * h * 2
+    if op == "layernorm":
+        return B * h * 4 + B * h * 2 + 2 * h * 2
+    if op == "embed":
+        return B * h * 2 + B * h * 4 + 2 * h * 2 + B * 4
+    if op == "head":
+        return V * h * 2 + B * h * 2 + B * 4
+    raise ValueError(op)
 
 
-# ------------------------------------------------------------------ measured DRAM traffic
-# The LM head + argmax runs on the tensor-core decode kernel from 8 sequences
-# on (unless disabled), else on the weight-streaming kernel.
-HEAD_KERNELS = {
-    "gemv_tc": ("gemv_tc_kernel (tensor-core LM head + argmax)",
-                ["k_gemv_tc.cu", "tc_ops.cuh", "tile_ops.cuh", "common.cuh", "kernels.h"]),
-    "linear": ("linear_kernel (weight-streaming LM head + argmax)",
-               ["k_linear.cu", "tile_ops.cuh", "common.cuh", "kernels.h"]),
+OP_NAMES = {"embed": "embedding gather + LN", "layernorm": "LayerNorm",
+            "qkv": "fused QKV + bias + K/V append", "attn": "split-KV ALiBi decode attention",
+            "dense": "attention output projection + bias + residual",
+            "up": "MLP up + bias + GeLU", "down": "MLP down + bias + residual",
+            "head": "tied LM head + argmax"}
+KERNEL_SOURCES = {
+    "gemv_tc_kernel": ["k_gemv_tc.cu", "tc_ops.cuh", "tile_ops.cuh", "common.cuh", "kernels.h"],
+    "linear_kernel": ["k_linear.cu", "tile_ops.cuh", "common.cuh", "kernels.h"],
+    "attn_decode_kernel": ["k_attn.cu", "attn_ops.cuh", "common.cuh", "kernels.h"],
+    "layernorm_kernel": ["k_norm.cu", "norm_ops.cuh", "common.cuh", "kernels.h"],
+    "embed_kernel": ["k_norm.cu", "norm_ops.cuh", "common.cuh", "kernels.h"],
 }
-TC_HEAD_MIN_B = 8
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lm_head_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def head_kernel(B: int, tc: bool) -> str:
-    return "gemv_tc" if tc and B >= TC_HEAD_MIN_B else "linear"
-
-
-def head_source_digest(kernel: str) -> str:
+def kernel_source_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in HEAD_KERNELS[kernel][1]:
+    for f in KERNEL_SOURCES.get(kernel, []):
         with open(os.path.join(ROOT, "bloom_decoder_token_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def head_traffic(sh: synth.Shape, B: int, kernel: str):
-    """dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch as an
-    ncu capture recorded it for this workload and kernel, or None when there is
-    no capture for it or the kernel's sources changed since."""
+def recorded_traffic(op: str, kernel: str, workload: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum of one launch of this
+    operation's kernel as an ncu capture recorded it for this workload, or None
+    when there is none or the kernel's sources changed since."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    d = json.load(open(TRAFFIC_FILE)).get("kernels", {}).get(kernel)
-    if not d or d.get("kernel_source_sha256") != head_source_digest(kernel):
+    d = json.load(open(TRAFFIC_FILE)).get("kernels", {}).get(f"{op}/{kernel}")
+    if not d or d.get("kernel_source_sha256") != kernel_source_digest(kernel):
         return None
-    return d.get("bytes_per_launch", {}).get(f"{sh.name}/B{B}")
-
-
-def measure_head(gm, sh, B, dev, stream, reps=50):
-    """Dominant kernel: the tied LM head + argmax (largest single weight stream),
-    timed alone with CUDA events on its stream."""
-    xn = torch.randn(B, sh.hidden, device=dev).to(torch.bfloat16)
-    ht = torch.empty(B, dtype=torch.int32, device=dev)
-    for _ in range(3):
-        gm.lm_head(xn, ht)
-    torch.cuda.synchronize(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        gm.lm_head(xn, ht)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    head_ms = a.elapsed_time(b) / reps
-    head_bytes = head_launch_bytes(sh, B)
-    return head_ms, head_bytes, head_bytes / (head_ms / 1e3) / 1e9
-
-
-def run_roofline_only(args, sh):
-    """Only the dominant kernel's measurement (the command an ncu capture of its
-    DRAM counters runs)."""
-    import bloom_decoder_token_gb300 as bg
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    B = sh.batch
-    w = synth.make_weights(sh.with_(n_layer=1), seed=0, device=dev)
-    gm = bg.Model(w, max_batch=B, max_tokens=B * sh.prompt, max_seq=sh.max_seq,
-                  flags=bg.FLAG_NO_TC_GEMM if args.no_tc_gemm else 0)
-    kernel = head_kernel(B, not args.no_tc_gemm)
-    head_ms, head_bytes, head_gbs = measure_head(gm, sh, B, dev, torch.cuda.current_stream(dev))
-    hbm, src = peaks()
-    print(json.dumps({"roofline_only": True, "workload": f"{sh.name}/B{B}", "kernel": kernel,
-                      "launch_ms": head_ms, "bytes_per_launch": head_bytes,
-                      "achieved_gbs": head_gbs, "frac": head_gbs / hbm, "peak_source": src,
-                      "kernel_source_sha256": head_source_digest(kernel)}), flush=True)
-    gm.close()
+    return d.get("bytes_per_launch", {}).get(workload)
 
 
 # ------------------------------------------------------------------ clocks
@@ -187,22 +177,26 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_sample(sh, w_host, ids, mask, decode_steps):
-    """Time the oracle on a bounded sample: prefill + `decode_steps` steps."""
+def oracle_sample(sh, w_host, ids, mask, rows, decode_steps):
+    """Time the oracle on a bounded sample of the job: the prefill of the first
+    `rows` prompts, then `decode_steps` decode steps of those rows.  Returns
+    (seconds of the sample, extrapolated seconds of the whole job, threads):
+    the oracle's cost is linear in rows, so the job (B rows, one prefill and
+    new_tokens - 1 decode steps) takes B / rows * (prefill + (new_tokens - 1)
+    * mean decode step)."""
     import oracle
     om = oracle.Model(w_host)
     B, T = ids.shape
-    seqs = om.new_seqs(B, T + decode_steps + 1)
+    seqs = om.new_seqs(rows, T + decode_steps + 1)
     t0 = time.perf_counter()
-    lg = om.prefill(seqs, ids.numpy(), mask.numpy())
+    lg = om.prefill(seqs, ids[:rows].numpy(), mask[:rows].numpy())
+    t1 = time.perf_counter()
     for _ in range(decode_steps):
         lg = om.decode(seqs, lg.argmax(axis=1).astype("int32"))
-    dt = time.perf_counter() - t0
-    return dt, B * (1 + decode_steps), oracle.num_threads()
-
-
-def host_weights(w):
-    return w.to("cpu")
+    t2 = time.perf_counter()
+    step = (t2 - t1) / max(decode_steps, 1)
+    job = B / rows * ((t1 - t0) + (sh.new_tokens - 1) * step)
+    return t2 - t0, job, oracle.num_threads()
 
 
 # ------------------------------------------------------------------ distributed
@@ -242,37 +236,147 @@ def sum_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, sh):
+    """The CPU oracle as it stands, on the host cores: every step is one
+    bounded sample of the workload (the prefill of one prompt and
+    `ref_decode_steps` decode steps of it), extrapolated to the whole job."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     ids, mask = synth.make_prompts(sh, seed=0)
     w = synth.make_weights(sh, seed=0, device="cpu")
     steps = args.ref_decode_steps
-    times = []
+    samples, jobs = [], []
+    cores = 0
     for i in range(args.warmup + args.steps):
-        dt, ntok, cores = oracle_sample(sh, w, ids, mask, steps)
+        dt, job, cores = oracle_sample(sh, w, ids, mask, 1, steps)
         if i >= args.warmup:
-            times.append(dt)
-    per = sum(times) / len(times)
+            samples.append(dt)
+            jobs.append(job)
     B = ids.shape[0]
-    value = B * (1 + steps) / per
+    job = sum(jobs) / len(jobs)
+    value = B * sh.new_tokens / job
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,0.02) weights, "
-        "random prompts)",
-        "config": {"workload": sh.name, "batch": B, "prompt": int(ids.shape[1]),
-                   "tokens_per_step": 1 + steps},
+        "ms_per_step": 1e3 * sum(samples) / len(samples), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,0.02) weights, random prompts)",
+        "config": workload_config(sh, B, int(ids.shape[1]), 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"prefill + {steps} decode steps of the {sh.name} workload "
-                                   f"(B={B}) per step"},
+                         "sample": f"per step: prefill of 1 of the {B} prompts + {steps} decode "
+                                   f"steps of it, float64 oracle; tokens/s of the whole job "
+                                   f"extrapolated linearly in rows and decode steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+def workload_config(sh, B, T, world):
+    return {"workload": f"{sh.name}: {sh.n_layer} layers, h {sh.hidden}, {sh.n_head} heads x "
+                        f"{sh.head_dim}, MLP {sh.ffn}, vocab {sh.vocab}"
+                        f"{', int8 weight-only block linears' if sh.int8 else ''}, batch {B}, "
+                        f"prompt {T}{' (left-padded, lengths 8..32)' if sh.ragged else ''}, "
+                        f"{sh.new_tokens} greedy tokens",
+            "batch": B, "prompt": T, "new_tokens": sh.new_tokens,
+            "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2: {weight_bytes(sh) / 1e9:.2f} GB of weights streamed "
+                  f"per decode step vs {L2_BYTES / 2 ** 20:.0f} MiB L2"}
+
+
 # ------------------------------------------------------------------ our arm
+def model_flags(args, bg):
+    return ((bg.FLAG_NO_PDL if args.no_pdl else 0) |
+            (bg.FLAG_NO_LN_FUSION if args.no_ln_fusion else 0) |
+            (bg.FLAG_NO_TC_GEMM if args.no_tc_gemm else 0))
+
+
+def time_decode_steps(gm, kv, tok, steps, stream, dev):
+    """Mean time of `steps` decode steps (graph replays) with CUDA events."""
+    gm.decode_step(kv, tok, tok)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(steps):
+        gm.decode_step(kv, tok, tok)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / steps
+
+
+def decode_series(gm, sh, batches, dev, stream, hbm):
+    """Decode step time of the model at several batch sizes: prefill of the
+    first B prompts of the workload, then the 99 decode steps of a generation
+    (every step reads one more key per sequence), timed as graph replays."""
+    out = {}
+    ids_all, mask_all = synth.make_prompts(sh.with_(batch=max(batches)), seed=0)
+    for B in batches:
+        ids, mask = ids_all[:B].to(dev), mask_all[:B].to(dev)
+        T = ids.shape[1]
+        n_steps = sh.new_tokens - 1
+        kv = gm.new_kv(B, T + sh.new_tokens)
+        tok = torch.empty(B, dtype=torch.int32, device=dev)
+        gm.prefill(kv, ids, mask, out_tokens=tok)
+        ms = time_decode_steps(gm, kv, tok, n_steps - 1, stream, dev)   # first step untimed
+        keys = T + sh.new_tokens // 2
+        nbytes = decode_step_bytes(sh, B, keys)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[str(B)] = {"decode_step_ms": ms, "ms_per_token": ms / B, "tokens_per_s": B / ms * 1e3,
+                       "decode_step_bytes": nbytes, "decode_hbm_gbs": gbs,
+                       "decode_hbm_frac": gbs / hbm}
+        del kv
+    return out
+
+
+def kernel_shares(gm, sh, B, T, dev, reps=3):
+    """Each operation's share of one decode step, timed launch by launch with
+    CUDA events on the step's stream (bloom_decode_profile: the same kernels
+    as a graph replay, each starting after its predecessor has finished), in
+    the middle of a generation (cache about half full).  Per (op, kernel):
+    launches, total ms (median over `reps` steps), share, algorithmic bytes per
+    launch and the bandwidth they imply."""
+    ids, mask = synth.make_prompts(sh.with_(batch=B), seed=0)
+    kv = gm.new_kv(B, T + sh.new_tokens)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    gm.prefill(kv, ids.to(dev), mask.to(dev), out_tokens=tok)
+    for _ in range(sh.new_tokens // 2 - 1):
+        gm.decode_step(kv, tok, tok)
+    keys = kv.len + 1
+    runs = [gm.decode_profile(kv, tok, tok) for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    per = {}
+    for i, (op, kern, _) in enumerate(runs[0]):
+        ms = statistics.median(r[i][2] for r in runs)
+        d = per.setdefault((op, kern), {"op": op, "kernel": kern, "launches": 0, "ms": 0.0})
+        d["launches"] += 1
+        d["ms"] += ms
+    total = sum(d["ms"] for d in per.values())
+    rows = []
+    for d in sorted(per.values(), key=lambda d: -d["ms"]):
+        nb = op_bytes(sh, B, d["op"], keys + 1)
+        per_launch = d["ms"] / d["launches"]
+        rows.append({**d, "share": d["ms"] / total, "ms_per_launch": per_launch,
+                     "bytes_per_launch": nb, "gbs": nb / (per_launch / 1e3) / 1e9})
+    return rows, total, keys
+
+
+def extra_stack(name, batches, dev, args, bg, hbm):
+    """Decode series of another preset (its own model, freed afterwards)."""
+    sh = synth.PRESETS[name]
+    ids, _ = synth.make_prompts(sh.with_(batch=max(batches)), seed=0)
+    T = ids.shape[1]
+    w = synth.make_weights(sh, seed=0, device=dev)
+    gm = bg.Model(w, max_batch=max(batches), max_tokens=max(batches) * T,
+                  max_seq=T + sh.new_tokens, flags=model_flags(args, bg))
+    stream = torch.cuda.current_stream(dev)
+    out = decode_series(gm, sh, batches, dev, stream, hbm)
+    gm.close()
+    del gm, w
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return {"workload": workload_config(sh, max(batches), T, 1)["workload"], "by_batch": out}
+
+
 def run_ours(args, sh):
     import bloom_decoder_token_gb300 as bg
 
@@ -284,12 +388,10 @@ def run_ours(args, sh):
     B, T = ids.shape
     n_new = sh.new_tokens
     S = T + n_new
+    series = SERIES_BATCHES if (sh.name == "7b1" and not args.no_extras) else ()
+    max_b = max((B,) + tuple(series))
     w = synth.make_weights(sh, seed=0, device=dev)
-    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S,
-                  flags=(bg.FLAG_NO_PDL if args.no_pdl else 0) |
-                  (bg.FLAG_NO_LN_FUSION if args.no_ln_fusion else 0) |
-                  (bg.FLAG_PERSISTENT if args.persistent else 0) |
-                  (bg.FLAG_NO_TC_GEMM if args.no_tc_gemm else 0))
+    gm = bg.Model(w, max_batch=max_b, max_tokens=max_b * T, max_seq=S, flags=model_flags(args, bg))
     kv = gm.new_kv(B, S)
     ids_d, mask_d = ids.to(dev), mask.to(dev)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
@@ -321,7 +423,7 @@ def run_ours(args, sh):
     tokens_all = sum_over_ranks(args.steps * B * n_new, world)
     value = tokens_all / (ms_total / 1e3)
 
-    # decode step alone: mean over the generation's 99 steps (graph replays)
+    # prefill alone, and the decode step as the rest of the generation
     prefill_ms = []
     for _ in range(3):
         a = torch.cuda.Event(enable_timing=True)
@@ -331,19 +433,17 @@ def run_ours(args, sh):
         b.record(stream)
         torch.cuda.synchronize(dev)
         prefill_ms.append(a.elapsed_time(b))
-        for i in range(1, n_new):
-            gm.decode_step(kv, tok, tok)
-    torch.cuda.synchronize(dev)
     pre_ms = min(prefill_ms)
     dec_ms = (ms_step - pre_ms) / (n_new - 1)
-    mean_keys = T + n_new / 2.0
-    step_bytes = decode_step_bytes(sh, B, int(round(mean_keys)))
     hbm, src = peaks()
+    step_bytes = decode_step_bytes(sh, B, T + n_new // 2)
     dec_gbs = step_bytes / (dec_ms / 1e3) / 1e9
 
-    head_ms, head_bytes, head_gbs = measure_head(gm, sh, B, dev, stream)
-    kernel = head_kernel(B, not args.no_tc_gemm)
-    traffic = args.head_traffic if args.head_traffic is not None else head_traffic(sh, B, kernel)
+    # per-operation shares of a decode step; the roofline kernel is the largest
+    shares, prof_total, prof_keys = kernel_shares(gm, sh, B, T, dev)
+    top = shares[0]
+    workload_key = f"{sh.name}/B{B}"
+    traffic = recorded_traffic(top["op"], top["kernel"], workload_key)
 
     # end to end through the public API with host buffers
     ids_h = ids.contiguous().pin_memory()
@@ -359,19 +459,33 @@ def run_ours(args, sh):
     t1 = time.perf_counter()
     e2e_s = max_over_ranks(t1 - t0, world)
     e2e_value = tokens_all / e2e_s
+    del kv2
 
     launches_prefill = 2 + 7 * sh.n_layer + 2
     launches = args.steps * (launches_prefill + (n_new - 1) * gm.decode_launches(B))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        wh = host_weights(w)
-        steps = args.cpu_decode_steps
-        dt, ntok, cores = oracle_sample(sh, wh, ids, mask, steps)
-        cpu = {"value": ntok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"prefill + {steps} decode steps of the same workload (B={B}), "
-                         f"{dt:.1f} s, fp64"}
+        wh = w.to("cpu")
+        rows, steps = 1, args.cpu_decode_steps
+        dt, job, cores = oracle_sample(sh, wh, ids, mask, rows, steps)
+        cpu = {"value": B * n_new / job, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"prefill of {rows} of the {B} prompts + {steps} decode steps of it "
+                         f"({dt:.1f} s, float64 oracle); tokens/s of the whole job extrapolated "
+                         f"linearly in rows and decode steps"}
         del wh
+
+    extras = {}
+    if series:
+        extras["decode_by_batch"] = decode_series(gm, sh, series, dev, stream, hbm)
+    gm.close()
+    del gm, kv
+    torch.cuda.synchronize(dev)
+    if not args.no_extras and sh.name == "7b1":
+        del w
+        torch.cuda.empty_cache()
+        extras["int8_7b1"] = extra_stack("7b1int8", (1, 8, 32, 128), dev, args, bg, hbm)
+        extras["cfg_176b14"] = extra_stack("176b14", (1, 8, 32), dev, args, bg, hbm)
 
     if rank == 0:
         line = {
@@ -380,32 +494,33 @@ def run_ours(args, sh):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int8" if sh.int8 else "bf16",
             "data": "synthetic: seeded N(0,0.02) bf16 weights, biases 0, LN 1/0, random prompts",
-            "config": {"workload": f"{sh.name}: {sh.n_layer} layers, h {sh.hidden}, "
-                                   f"{sh.n_head} heads, vocab {sh.vocab}, batch {B}, prompt {T}"
-                                   f"{' (left-padded, lengths 8..32)' if sh.ragged else ''}, "
-                                   f"{n_new} greedy tokens",
-                       "batch": B, "prompt": T, "new_tokens": n_new,
-                       "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2: {weight_bytes(sh) / 1e9:.2f} GB of "
-                             f"weights streamed per decode step vs {L2_BYTES / 2**20:.0f} MiB L2"},
+            "config": workload_config(sh, B, T, world),
             "ms_per_token": ms_total / (args.steps * B * n_new),
             "decode_step_ms": dec_ms, "prefill_ms": pre_ms,
             "decode_step_bytes": step_bytes,
             "decode_hbm_gbs": dec_gbs,
             "decode_hbm_frac": dec_gbs / hbm,
-            "roofline": {"bound": "hbm", "kernel": HEAD_KERNELS[kernel][0],
-                         "achieved": head_gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": head_gbs / hbm, "traffic": traffic,
-                         "peak_source": src, "bytes_per_launch": head_bytes,
-                         "launch_ms": head_ms},
+            "roofline": {"bound": "hbm", "kernel": f"{top['kernel']} ({OP_NAMES[top['op']]})",
+                         "achieved": top["gbs"], "peak": hbm, "unit": "GB/s",
+                         "frac": top["gbs"] / hbm, "traffic": traffic, "peak_source": src,
+                         "bytes_per_launch": top["bytes_per_launch"],
+                         "launch_ms": top["ms_per_launch"], "step_share": top["share"],
+                         "timing": "CUDA events on the decode stream, one event per launch, "
+                                   "launches serialised (bloom_decode_profile)"},
+            "kernel_shares": {"workload": workload_key, "keys": prof_keys,
+                              "serialised_step_ms": prof_total,
+                              "rows": [{k: r[k] for k in ("op", "kernel", "launches", "ms",
+                                                          "share", "ms_per_launch",
+                                                          "bytes_per_launch", "gbs")}
+                                       for r in shares]},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": B * T * 5, "d2h_bytes_per_step": n_new * B * 4},
             "gpu_launches": launches,
             "clocks": clocks,
+            **extras,
         }
         print(json.dumps(line), flush=True)
-    gm.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -416,31 +531,27 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="560m", choices=sorted(synth.PRESETS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.PRESETS))
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--new-tokens", type=int, default=None)
     ap.add_argument("--layers", type=int, default=None, help="decoder layers (default: the preset's)")
     ap.add_argument("--prompt", type=int, default=None, help="padded prompt length (default: the preset's)")
-    ap.add_argument("--cpu-decode-steps", type=int, default=8)
+    ap.add_argument("--cpu-decode-steps", type=int, default=4)
     ap.add_argument("--ref-decode-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the workload itself (no batch series, int8 or 176B-shape keys)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     ap.add_argument("--no-ln-fusion", action="store_true", help="separate LayerNorm kernels")
-    ap.add_argument("--persistent", action="store_true",
-                    help="decode steps as one persistent cooperative launch (batches <= 16)")
     ap.add_argument("--no-tc-gemm", action="store_true",
-                    help="prefill linears on the weight-streaming kernel instead of tcgen05")
-    ap.add_argument("--head-traffic", type=float, default=None,
-                    help="dram bytes per LM-head launch from an ncu capture of this kernel "
-                         "(default: the recorded capture, if the kernel is unchanged)")
-    ap.add_argument("--roofline-only", action="store_true",
-                    help="only time the dominant kernel (LM head + argmax) and print its line")
+                    help="every linear on the weight-streaming kernel instead of tcgen05")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     sh = synth.PRESETS[args.config]
-    if args.batch:
-        sh = sh.with_(batch=args.batch)
+    batch = args.batch or DEFAULT_BATCH.get(args.config)
+    if batch:
+        sh = sh.with_(batch=batch)
     if args.new_tokens:
         sh = sh.with_(new_tokens=args.new_tokens)
     if args.layers:
@@ -449,8 +560,6 @@ def main():
         sh = sh.with_(prompt=args.prompt)
     if args.impl == "reference":
         run_reference(args, sh)
-    elif args.roofline_only:
-        run_roofline_only(args, sh)
     else:
         run_ours(args, sh)
 

@@ -27,7 +27,10 @@ FLAG_NO_GRAPH = 1
 FLAG_NO_PDL = 2
 FLAG_NO_LN_FUSION = 4
 FLAG_NO_TC_GEMM = 8
-FLAG_PERSISTENT = 16
+
+OPS = ("embed", "layernorm", "qkv", "attn", "dense", "up", "down", "head")
+KERNELS = ("embed_kernel", "layernorm_kernel", "linear_kernel", "gemv_tc_kernel",
+           "gemm_tc_kernel", "attn_decode_kernel", "attn_prefill_kernel")
 
 P = C.c_void_p
 I32 = C.c_int32
@@ -72,6 +75,7 @@ _SIGS = {
     "bloom_decode_step": (I32, [P, C.POINTER(KVC), P, P, P, P]),
     "bloom_generate": (I32, [P, C.POINTER(KVC), P, P, I32, I32, I32, P, P]),
     "bloom_check_device": (I32, [P, P]),
+    "bloom_decode_profile": (I32, [P, C.POINTER(KVC), P, P, P, P, I32, P, P]),
     "bloom_destroy": (I32, [P]),
     "bloom_last_error": (C.c_char_p, []),
     "bloom_decode_launches": (I32, [P, I32]),
@@ -233,6 +237,19 @@ class Model:
         check(lib().bloom_generate(self.h, C.byref(kv.c), _p(tokens_host), _p(mask_host), B, T,
                                    n_new, _p(out_host), _stream(stream)))
         return out_host
+
+    def decode_profile(self, kv: KV, next_tokens, out_tokens=None, cap: int = 4096, stream=None):
+        """One decode step launched kernel by kernel with an event after each;
+        returns [(op, kernel, ms)] in launch order (names in OPS / KERNELS)."""
+        if out_tokens is None:
+            out_tokens = torch.empty(kv.batch, dtype=torch.int32, device=self.device)
+        codes = (C.c_int32 * cap)()
+        ms = (C.c_float * cap)()
+        n = C.c_int32(0)
+        check(lib().bloom_decode_profile(self.h, C.byref(kv.c), _p(next_tokens), _p(out_tokens),
+                                         codes, ms, cap, C.byref(n), _stream(stream)))
+        return [(OPS[codes[i] & 0xff], KERNELS[codes[i] >> 8], float(ms[i]))
+                for i in range(n.value)]
 
     def check_device(self, stream=None):
         check(lib().bloom_check_device(self.h, _stream(stream)))

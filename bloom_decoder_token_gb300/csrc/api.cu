@@ -77,12 +77,16 @@ static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq) {
 }
 
 // ----------------------------------------------------------------- model
+// A captured decode step.  The graph bakes in every address and stride of the
+// cache layout, so it is keyed by the whole cache descriptor (buffer, bytes,
+// batch, max_seq) and the step's token / logit buffers.
 struct GraphEntry {
     void *kvbuf;
+    size_t kvbytes;
+    int B, max_seq;
     const void *next;
     void *out;
     void *logits;
-    int B;
     cudaGraphExec_t exec;
 };
 
@@ -93,17 +97,6 @@ struct TcMap {
 enum { TC_QKV = 0, TC_O = 1, TC_UP = 2, TC_DOWN = 3, TC_PER_LAYER = 4 };
 enum { TC_X_A = 0, TC_X_O = 1, TC_X_U = 2 };
 constexpr int kTcNtClasses = 5;   // decode token columns 16, 32, 64, 128, 256
-
-// Phase table of the persistent decode step for one set of step buffers.
-struct PlanEntry {
-    void *kvbuf;
-    const void *next;
-    void *out;
-    void *logits;
-    int B;
-    PersistPhase *phases;   // device copy, then the stream table (PersistStream[n])
-    int n;
-};
 
 struct bloom_model {
     bloom_config cfg;
@@ -132,28 +125,18 @@ struct bloom_model {
     bool tc = false;
     std::vector<TcMap> wmaps;
     TcMap xmaps[3];
-    // tensor-core LM head (decode steps of >= kTcDecodeMinM sequences): the
+    // tensor-core LM head (decode steps, see use_tc_head): the
     // embedding's map (box 128 rows) and the ln_f output's maps per token-column class
     bool tcd = false;
     TcMap head_wmap;
     TcMap head_xmaps[kTcNtClasses];
-    // the bf16 block linears of decode steps of >= kTcDecodeBlockMinM sequences on
+    // the bf16 block linears of decode steps (see use_tc_linear) on
     // the tensor cores: weight maps [layer][TC_*] (box 128 rows), activation maps
-    // [TC_X_*][token-column class], split-K partial tiles and tickets
+    // [TC_X_*][token-column class]
     bool tcb = false;
     std::vector<TcMap> dwmaps;
     TcMap dxmaps[3][kTcNtClasses];
-    void *dscratch = nullptr;
-    float *dpart = nullptr;
-    int *dticket = nullptr;
-    // persistent decode step: grid (0 = not available), barrier words, phase tables
-    int pgrid = 0;
-    int pmax_phases = 0;
-    unsigned *pbar = nullptr;
-    void *pscratch = nullptr;   // partial tiles + row-group tickets of the persistent step
-    float *ppart = nullptr;
-    int *pticket = nullptr;
-    std::vector<PlanEntry> plans;
+
 };
 
 static int attn_splits(const bloom_model *m, int B, int max_seq) {
@@ -204,9 +187,6 @@ extern "C" bloom_status bloom_destroy(bloom_model *m) {
     if (!m) return BLOOM_OK;
     cudaSetDevice(m->dev);
     for (auto &g : m->graphs) cudaGraphExecDestroy(g.exec);
-    for (auto &p : m->plans) cudaFree(p.phases);
-    if (m->pscratch) cudaFree(m->pscratch);
-    if (m->dscratch) cudaFree(m->dscratch);
     if (m->cap) cudaStreamDestroy(m->cap);
     if (m->ws) cudaFree(m->ws);
     delete m;
@@ -262,7 +242,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
                  o_ap = take(MB * n * kMaxSplits * (d + 2) * 4), o_at = take(MB * n * 4),
                  o_err = take(4), o_last = take(MB * 4), o_tok = take(MB * 4),
                  o_gen = take((size_t)cfg->max_seq * MB * 4), o_ptok = take(MT * 4),
-                 o_pmask = take(MT), o_pbar = take(16);
+                 o_pmask = take(MT);
     m->ws_bytes = off;
     e = cudaMalloc(&m->ws, m->ws_bytes);
     if (e != cudaSuccess) {
@@ -288,7 +268,6 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     m->gen = (int32_t *)(base + o_gen);
     m->ptok = (int32_t *)(base + o_ptok);
     m->pmask = (uint8_t *)(base + o_pmask);
-    m->pbar = (unsigned *)(base + o_pbar);
     // ALiBi slopes, once: largest power of two p <= n heads gets 2^(-8i/p),
     // i = 1..p; the remaining heads take 2^(-8i/(2p)) for odd i = 1, 3, ...
     std::vector<float> sl(n);
@@ -303,8 +282,8 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         linear_prepare() != cudaSuccess) {
         st2 = fail(BLOOM_E_CUDA, "workspace init: %s", cudaGetErrorString(cudaGetLastError()));
     }
-    // the LM head of decode steps of >= kTcDecodeMinM sequences on the tensor cores
-    if (!st2 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_batch >= kTcDecodeMinM) {
+    // the LM head of decode steps on the tensor cores
+    if (!st2 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM)) {
         bool ok = gemm_map_bytes() == sizeof(TcMap) &&
                   gemm_make_map(m->head_wmap.b, w->word_emb, cfg->vocab, h, gemv_tc_box_rows_w());
         const int ntmax = gemv_tc_nt(cfg->max_batch);
@@ -317,7 +296,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         else
             m->tcd = true;
     }
-    if (!st2 && m->tcd && !i8 && cfg->max_batch >= kTcDecodeBlockMinM) {
+    if (!st2 && m->tcd && !i8) {
         const int F = cfg->ffn;
         const int ntmax = gemv_tc_nt(cfg->max_batch);
         bool ok = true;
@@ -335,45 +314,10 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
             ok = gemm_make_map(m->dxmaps[TC_X_A][ci].b, m->a, cfg->max_batch, h, 16 << ci) &&
                  gemm_make_map(m->dxmaps[TC_X_O][ci].b, m->o, cfg->max_batch, h, 16 << ci) &&
                  gemm_make_map(m->dxmaps[TC_X_U][ci].b, m->u, cfg->max_batch, F, 16 << ci);
-        // split-K scratch for the largest of the four shapes
-        const int shapes[4][2] = {{3 * h, h}, {h, h}, {F, h}, {h, F}};
-        size_t pf = 0;
-        int tk = 0;
-        for (const auto &sh : shapes) {
-            pf = std::max(pf, gemv_tc_part_floats(sh[0], sh[1], cfg->max_batch, m->num_sms));
-            tk = std::max(tk, (sh[0] + 127) / 128);
-        }
-        const size_t pb = align256(pf * 4);
-        const size_t bytes = pb + (size_t)tk * 4;
-        if (!ok) {
+        if (!ok)
             st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the decode linears could not be encoded");
-        } else if (cudaMalloc(&m->dscratch, bytes) != cudaSuccess ||
-                   cudaMemset(m->dscratch, 0, bytes) != cudaSuccess) {
-            st2 = fail(BLOOM_E_OOM, "decode-linear scratch of %zu bytes", bytes);
-        } else {
-            m->dpart = (float *)m->dscratch;
-            m->dticket = (int *)((char *)m->dscratch + pb);
+        else
             m->tcb = true;
-        }
-    }
-    if (!st2 && (cfg->flags & BLOOM_FLAG_PERSISTENT)) {
-        m->pgrid = persist_grid(i8);   // 0: no cooperative launch of one block per SM here
-        m->pmax_phases = m->pgrid > 0 ? persist_max_phases(i8) : 0;
-        cudaGetLastError();
-        if (m->pgrid > 0) {
-            int groups = (3 * h + 7) / 8;
-            groups = std::max(groups, (F + 7) / 8);
-            groups = std::max(groups, (cfg->vocab + 7) / 8);
-            const size_t pb = align256(persist_part_bytes(m->pgrid));
-            const size_t bytes = pb + (size_t)groups * 4;
-            if (cudaMalloc(&m->pscratch, bytes) != cudaSuccess ||
-                cudaMemset(m->pscratch, 0, bytes) != cudaSuccess) {
-                st2 = fail(BLOOM_E_OOM, "persistent-step scratch of %zu bytes", bytes);
-            } else {
-                m->ppart = (float *)m->pscratch;
-                m->pticket = (int *)((char *)m->pscratch + pb);
-            }
-        }
     }
     // TMA descriptors of every bf16 weight and of the activations the prefill GEMMs read
     if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_tokens >= kTcMinM) {
@@ -428,6 +372,19 @@ extern "C" bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, s
     const KvLayout L = kv_layout(m->cfg, batch, max_seq);
     if (bytes < L.total) return fail(BLOOM_E_INVALID, "kv buffer %zu < %zu bytes", bytes, L.total);
     cudaStream_t s = (cudaStream_t)stream;
+    // graphs captured on a cache that overlaps this buffer describe a layout that
+    // no longer exists (the caller re-bound or re-allocated the memory)
+    for (size_t i = 0; i < m->graphs.size();) {
+        const GraphEntry &g = m->graphs[i];
+        const char *a0 = (const char *)g.kvbuf, *a1 = a0 + g.kvbytes;
+        const char *b0 = (const char *)buf, *b1 = b0 + bytes;
+        if (a0 < b1 && b0 < a1) {
+            cudaGraphExecDestroy(g.exec);
+            m->graphs.erase(m->graphs.begin() + (long)i);
+        } else {
+            ++i;
+        }
+    }
     CK(cudaMemsetAsync(buf, 0, L.pos, s));
     CK(cudaMemsetAsync((char *)buf + L.pos, 0xff, L.k - L.pos, s));
     kv->buf = buf;
@@ -472,12 +429,18 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
     return a;
 }
 
-// A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
-// kTcMinM tokens or more, else the weight-streaming kernel.
+// Whether the LayerNorm feeding `a` would be fused into the weight-streaming
+// kernel (decode, 1-2 rows).  There the fused launch beats the tensor-core
+// kernel plus a LayerNorm launch, so QKV, up and the head stay on it.
+static bool prefers_ln_fusion(const bloom_model *m, const LinearArgs &a) {
+    return !(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION) && linear_can_fuse_ln(a) &&
+           (a.epi == EPI_QKV || a.epi == EPI_GELU || a.epi == EPI_ARGMAX);
+}
+
 // The LM head + argmax on the tensor cores (one pass over the embedding; no K split).
 static bool use_tc_head(const bloom_model *m, const LinearArgs &a) {
-    return m->tcd && a.epi == EPI_ARGMAX && a.M >= kTcDecodeMinM && a.M <= m->cfg.max_batch &&
-           !a.ln_x;
+    return m->tcd && a.epi == EPI_ARGMAX && a.M >= 3 && a.M <= m->cfg.max_batch && !a.ln_x &&
+           !prefers_ln_fusion(m, a);
 }
 
 // Index of the activation map whose box covers nt token columns (16 << index).
@@ -487,49 +450,86 @@ static int nt_class(int nt) {
     return ci;
 }
 
+// ----------------------------------------------------------------- launch profile
+// bloom_decode_profile records a CUDA event after every launch of one decode
+// step; each launch site calls prof_mark with its operation and kernel.
+struct LaunchProfile {
+    std::vector<cudaEvent_t> ev;
+    std::vector<int32_t> code;
+    cudaError_t err = cudaSuccess;
+};
+static thread_local LaunchProfile *g_prof = nullptr;
+
+static void prof_mark(cudaStream_t s, int op, int kernel) {
+    if (!g_prof) return;
+    cudaEvent_t e = nullptr;
+    cudaError_t r = cudaEventCreate(&e);
+    if (r == cudaSuccess) r = cudaEventRecord(e, s);
+    if (r != cudaSuccess) {
+        if (e) cudaEventDestroy(e);
+        g_prof->err = r;
+        return;
+    }
+    g_prof->ev.push_back(e);
+    g_prof->code.push_back(op | (kernel << 8));
+}
+
+static GemvTcArgs tc_args(const bloom_model *m, const LinearArgs &a) {
+    GemvTcArgs g;
+    g.a = a;
+    g.splits = gemv_tc_splits(a.N, a.K, a.M, a.epi, m->num_sms);
+    return g;
+}
+
 static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t s) {
     const int nt = gemv_tc_nt(a.M);
     const int ci = nt_class(nt);
-    GemvTcArgs g;
-    g.a = a;
-    g.splits = 1;
-    return launch_gemv_tc(m->head_wmap.b, m->head_xmaps[ci].b, g, nt, s);
+    return launch_gemv_tc(m->head_wmap.b, m->head_xmaps[ci].b, tc_args(m, a), nt, s);
 }
 
-// A decode block linear on the tensor-core decode kernel: bf16 weights, at least
-// kTcDecodeBlockMinM sequences, and a matrix that is wide (>= 8192 rows) or long
-// (K >= 8192), or at least 64 sequences.  Measured per kernel on GB300 (7b1
-// shapes, back-to-back launches): at 8-64 tokens it beats the weight-streaming
-// kernel on the QKV, up and down matrices (32 tokens: 23 / 26 / 43 us vs
-// 33 / 49 / 48 us; 8 and 16 tokens share its 16-column tile: 21 / 25 / 33 us
-// vs 22 / 31 / 35 us at 8), not on the 4096 x 4096 dense one below 64 tokens.
-constexpr int kTcBlockWide = 8192;   // rows or K from which a block linear qualifies
-constexpr int kTcBlockAnyM = 64;     // sequences from which every block linear does
+// A decode block linear on the tensor-core decode kernel: bf16 weights, from
+// kTcBlockMinM sequences.  Measured per kernel on GB300 (7b1 shapes, launches
+// back to back, 8 / 32 tokens, tensor-core kernel vs weight-streaming kernel):
+// QKV 18.9 / 21.4 vs 21.8 / 33.0 us, dense 9.3 / 11.9 vs 9.6 / 14.3, up
+// 23.9 / 26.4 vs 30.4 / 48.6, down 24.8 / 28.2 vs 34.3 / 48.5.  At one or two
+// sequences the whole step stays on the weight-streaming kernel (QKV and up
+// with the LayerNorm fused): its CTAs take no shared memory, so each launch
+// becomes resident beside its predecessor and starts streaming early; a
+// tensor-core kernel between them (two 108 KB CTAs per SM) blocks that, and
+// the 7b1 step at one sequence took 4.17 ms instead of 3.18.
+constexpr int kTcBlockMinM = 3;
 static bool use_tc_linear(const bloom_model *m, const LinearArgs &a) {
-    return m->tcb && a.T == 0 && !a.int8 && !a.ln_x && a.M >= kTcDecodeBlockMinM &&
-           a.M <= m->cfg.max_batch &&
-           (a.N >= kTcBlockWide || a.K >= kTcBlockWide || a.M >= kTcBlockAnyM);
+    return m->tcb && a.T == 0 && !a.int8 && !a.ln_x && a.M >= kTcBlockMinM &&
+           a.M <= m->cfg.max_batch && !prefers_ln_fusion(m, a);
 }
 
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
 // kTcMinM tokens or more, the tensor-core decode kernel where use_tc_linear
 // says so, else the weight-streaming kernel.
+static int wmap_op(int wmap) {
+    return wmap == TC_QKV ? BLOOM_OP_QKV : wmap == TC_O ? BLOOM_OP_DENSE
+                                         : wmap == TC_UP ? BLOOM_OP_UP : BLOOM_OP_DOWN;
+}
+
 static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wmap, int xmap,
                               cudaStream_t s) {
-    if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x)
-        return launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
-    if (use_tc_linear(m, a)) {
+    cudaError_t e;
+    int kernel;
+    if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x) {
+        e = launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
+        kernel = BLOOM_KERNEL_GEMM_TC;
+    } else if (use_tc_linear(m, a)) {
         const int nt = gemv_tc_nt(a.M);
         const int ci = nt_class(nt);
-        GemvTcArgs g;
-        g.a = a;
-        g.splits = gemv_tc_splits(a.N, a.K, m->num_sms, a.epi);
-        g.part = m->dpart;
-        g.ticket = m->dticket;
-        return launch_gemv_tc(m->dwmaps[(size_t)l * TC_PER_LAYER + wmap].b, m->dxmaps[xmap][ci].b,
-                              g, nt, s);
+        e = launch_gemv_tc(m->dwmaps[(size_t)l * TC_PER_LAYER + wmap].b, m->dxmaps[xmap][ci].b,
+                           tc_args(m, a), nt, s);
+        kernel = BLOOM_KERNEL_GEMV_TC;
+    } else {
+        e = launch_linear(a, m->num_sms, s);
+        kernel = BLOOM_KERNEL_STREAM;
     }
-    return launch_linear(a, m->num_sms, s);
+    if (e == cudaSuccess) prof_mark(s, wmap_op(wmap), kernel);
+    return e;
 }
 
 // Whether the LayerNorm feeding linear `a` runs inside it: allowed by the flags
@@ -552,8 +552,11 @@ static cudaError_t fused_ln(bloom_model *m, LinearArgs &a, const float *x, const
         a.ln_eps = m->cfg.ln_eps;
         return cudaSuccess;
     }
-    return launch_layernorm_f32(x, (const uint16_t *)g, (const uint16_t *)b, a.M, a.K,
-                                m->cfg.ln_eps, const_cast<uint16_t *>(a.x), 1, nullptr, s);
+    const cudaError_t e = launch_layernorm_f32(x, (const uint16_t *)g, (const uint16_t *)b, a.M,
+                                               a.K, m->cfg.ln_eps, const_cast<uint16_t *>(a.x), 1,
+                                               nullptr, s);
+    if (e == cudaSuccess) prof_mark(s, BLOOM_OP_LAYERNORM, BLOOM_KERNEL_LAYERNORM);
+    return e;
 }
 
 // One decoder layer over M tokens.  Decode: M = B sequences, slot *len.
@@ -596,6 +599,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.ticket = m->attn_ticket;
         at.o = m->o;
         if ((e = launch_attn_decode(at, s))) return e;
+        prof_mark(s, BLOOM_OP_ATTN, BLOOM_KERNEL_ATTN);
     } else {
         AttnPrefillArgs at;
         at.q = m->q;
@@ -611,6 +615,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.scale = (float)(1.0 / sqrt((double)d));
         at.o = m->o;
         if ((e = launch_attn_prefill(at, s))) return e;
+        prof_mark(s, BLOOM_OP_ATTN, BLOOM_KERNEL_ATTN_PREFILL);
     }
     LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID32);
     od.out32 = x;
@@ -652,9 +657,13 @@ static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int strid
     } else if ((e = launch_layernorm_f32(x, (const uint16_t *)m->lnf_g, (const uint16_t *)m->lnf_b,
                                          B, c.hidden, c.ln_eps, m->xl, stride, last, s))) {
         return e;
+    } else {
+        prof_mark(s, BLOOM_OP_LAYERNORM, BLOOM_KERNEL_LAYERNORM);
     }
-    if (use_tc_head(m, a)) return run_tc_head(m, a, s);
-    return launch_linear(a, m->num_sms, s);
+    const bool tc = use_tc_head(m, a);
+    e = tc ? run_tc_head(m, a, s) : launch_linear(a, m->num_sms, s);
+    if (e == cudaSuccess) prof_mark(s, BLOOM_OP_HEAD, tc ? BLOOM_KERNEL_GEMV_TC : BLOOM_KERNEL_STREAM);
+    return e;
 }
 
 static cudaError_t enqueue_decode(bloom_model *m, const bloom_kv *kv, const int32_t *next,
@@ -668,20 +677,14 @@ static cudaError_t enqueue_decode(bloom_model *m, const bloom_kv *kv, const int3
                                  c.hidden, c.ln_eps, m->x, kp.len, kp.next_pos, kp.pos,
                                  kv->max_seq, m->err, s);
     if (e) return e;
+    prof_mark(s, BLOOM_OP_EMBED, BLOOM_KERNEL_EMBED);
     for (int l = 0; l < c.n_layer; ++l)
         if ((e = enqueue_layer(m, kp, B, kv->max_seq, l, B, 0, splits, m->x, s))) return e;
     return enqueue_head(m, m->x, B, 1, nullptr, out, logits, kp.len, kp.next_pos, s);
 }
 
-static bool use_persistent(const bloom_model *m, int B) {
-    // phases: embedding, 5 per layer (LayerNorms fused) or 7, ln_f + head
-    return m->pgrid > 0 && B >= 1 && B <= kPersistMaxM &&
-           1 + 7 * m->cfg.n_layer + 2 <= m->pmax_phases;
-}
-
 extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
     if (!m) return 0;
-    if (use_persistent(m, batch)) return 1;
     // embedding; per layer LN1, QKV, attention, dense, LN2, up, down; ln_f, head --
     // less the LayerNorm launches that the linear kernels absorb (ln_fuses)
     const bloom_config &c = m->cfg;
@@ -692,188 +695,6 @@ extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
     const int block_ln = (ln_fuses(m, qkv) ? 0 : 1) + (ln_fuses(m, up) ? 0 : 1);
     const int head_ln = ln_fuses(m, head) ? 0 : 1;
     return 1 + (5 + block_ln) * c.n_layer + 1 + head_ln;
-}
-
-// Key ranges per (sequence, head) in the persistent step: one visit of every
-// block covers all units.
-static int persist_splits(const bloom_model *m, int B, int max_seq) {
-    int s = m->pgrid / (B * m->cfg.n_head);
-    const int cap = (max_seq + 31) / 32;
-    if (s > cap) s = cap;
-    if (s > kMaxSplits) s = kMaxSplits;
-    return s < 1 ? 1 : s;
-}
-
-// The persistent step's phases: embedding; per layer LN1, QKV (+ K/V append),
-// attention, dense (+ residual), LN2, up (+ GeLU), down (+ residual); ln_f;
-// LM head + argmax.  The same operations and buffers as the per-launch step.
-static std::vector<PersistPhase> persist_plan(bloom_model *m, const bloom_kv *kv,
-                                              const int32_t *next, int32_t *out, float *logits) {
-    const bloom_config &c = m->cfg;
-    const KvPtrs kp = kv_ptrs(m, kv);
-    const int B = kv->batch, h = c.hidden, F = c.ffn, n = c.n_head, d = m->d;
-    const int i8 = c.weight_dtype == BLOOM_WEIGHT_INT8;
-    std::vector<PersistPhase> v;
-    PersistPhase e;
-    e.kind = PH_EMBED;
-    e.rows = B;
-    e.h = h;
-    e.eps = c.ln_eps;
-    e.g = (const uint16_t *)m->emb_ln_g;
-    e.b = (const uint16_t *)m->emb_ln_b;
-    e.tokens = next;
-    e.emb = (const uint16_t *)m->word_emb;
-    e.vocab = c.vocab;
-    e.emb_dst = m->x;
-    e.len = kp.len;
-    e.next_pos = kp.next_pos;
-    e.pos = kp.pos;
-    e.max_seq = kv->max_seq;
-    v.push_back(e);
-    auto ln = [&](const void *g, const void *b, uint16_t *dst) {
-        PersistPhase p;
-        p.kind = PH_LN;
-        p.rows = B;
-        p.h = h;
-        p.eps = c.ln_eps;
-        p.g = (const uint16_t *)g;
-        p.b = (const uint16_t *)b;
-        p.ln_src = m->x;
-        p.ln_dst = dst;
-        v.push_back(p);
-    };
-    auto lin = [&](const LinearArgs &a) {
-        PersistPhase p;
-        p.kind = PH_LINEAR;
-        p.lin = a;
-        persist_linear_geometry(p);
-        v.push_back(p);
-    };
-    // a linear layer fed by LN(x): the LayerNorm runs inside the linear phase
-    // (each block normalises the rows into its staged copy) when the rows are
-    // staged in shared memory, else as a phase of its own writing `dst`
-    auto lin_ln = [&](LinearArgs a, const void *g, const void *b, uint16_t *dst) {
-        PersistPhase p;
-        p.kind = PH_LINEAR;
-        p.lin = a;
-        persist_linear_geometry(p);
-        if (p.xs) {
-            p.lin.ln_x = m->x;
-            p.lin.ln_g = (const uint16_t *)g;
-            p.lin.ln_b = (const uint16_t *)b;
-            p.lin.ln_eps = c.ln_eps;
-        } else {
-            ln(g, b, dst);
-        }
-        v.push_back(p);
-    };
-    const int splits = persist_splits(m, B, kv->max_seq);
-    for (int l = 0; l < c.n_layer; ++l) {
-        const bloom_layer_weights &L = m->layers[l];
-        LinearArgs q = lin_args(L.qkv, i8, m->a, B, 3 * h, h, EPI_QKV);
-        q.q_out = m->q;
-        q.k_cache = kp.k + kp.layer_elems * l;
-        q.v_cache = kp.v + kp.layer_elems * l;
-        q.len_ptr = kp.len;
-        q.n_head = n;
-        q.head_dim = d;
-        q.max_seq = kv->max_seq;
-        q.err = m->err;
-        lin_ln(q, L.ln1_g, L.ln1_b, m->a);
-        PersistPhase at;
-        at.kind = PH_ATTN;
-        at.at.q = m->q;
-        at.at.k = q.k_cache;
-        at.at.v = q.v_cache;
-        at.at.pos = kp.pos;
-        at.at.slopes = m->slopes;
-        at.at.len_ptr = kp.len;
-        at.at.B = B;
-        at.at.n = n;
-        at.at.d = d;
-        at.at.max_seq = kv->max_seq;
-        at.at.splits = splits;
-        at.at.scale = (float)(1.0 / sqrt((double)d));
-        at.at.part = m->attn_part;
-        at.at.ticket = m->attn_ticket;
-        at.at.o = m->o;
-        v.push_back(at);
-        LinearArgs od = lin_args(L.o, i8, m->o, B, h, h, EPI_RESID32);
-        od.out32 = m->x;
-        lin(od);
-        LinearArgs up = lin_args(L.up, i8, m->a, B, F, h, EPI_GELU);
-        up.out = m->u;
-        lin_ln(up, L.ln2_g, L.ln2_b, m->a);
-        LinearArgs dn = lin_args(L.down, i8, m->u, B, h, F, EPI_RESID32);
-        dn.out32 = m->x;
-        lin(dn);
-    }
-    LinearArgs hd;
-    hd.w = m->word_emb;
-    hd.x = m->xl;
-    hd.M = B;
-    hd.N = c.vocab;
-    hd.K = h;
-    hd.epi = EPI_ARGMAX;
-    hd.logits = logits;
-    hd.best = m->best;
-    hd.ticket = m->head_ticket;
-    hd.out_tokens = out;
-    hd.len_inc = kp.len;
-    hd.next_pos = kp.next_pos;
-    lin_ln(hd, m->lnf_g, m->lnf_b, m->xl);
-    return v;
-}
-
-static bloom_status decode_persistent(bloom_model *m, const bloom_kv *kv, const int32_t *next,
-                                      int32_t *out, float *logits, cudaStream_t s) {
-    PlanEntry *pe = nullptr;
-    for (auto &p : m->plans)
-        if (p.kvbuf == kv->buf && p.next == next && p.out == out && p.logits == logits &&
-            p.B == kv->batch) {
-            pe = &p;
-            break;
-        }
-    if (!pe) {
-        const std::vector<PersistPhase> v = persist_plan(m, kv, next, out, logits);
-        std::vector<PersistStream> st(v.size());
-        for (size_t i = 0; i < v.size(); ++i) {
-            if (v[i].kind != PH_LINEAR) continue;
-            st[i].w = (const char *)v[i].lin.w;
-            st[i].tb = v[i].tb;
-            st[i].nbt = v[i].nbt;
-            st[i].N = v[i].lin.N;
-            st[i].row_bytes = v[i].lin.K * (v[i].lin.int8 ? 1 : 2);
-        }
-        const size_t pb = v.size() * sizeof(PersistPhase), sb = st.size() * sizeof(PersistStream);
-        std::vector<char> blob(pb + sb);
-        memcpy(blob.data(), v.data(), pb);
-        memcpy(blob.data() + pb, st.data(), sb);
-        PersistPhase *d = nullptr;
-        CK(cudaMalloc(&d, blob.size()));
-        cudaError_t e = cudaMemcpyAsync(d, blob.data(), blob.size(), cudaMemcpyHostToDevice, s);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // v is freed on return
-        if (e != cudaSuccess) {
-            cudaFree(d);
-            return fail(BLOOM_E_CUDA, "phase table: %s", cudaGetErrorString(e));
-        }
-        if (m->plans.size() >= 16) {
-            cudaFree(m->plans.front().phases);
-            m->plans.erase(m->plans.begin());
-        }
-        m->plans.push_back({kv->buf, next, out, logits, kv->batch, d, (int)v.size()});
-        pe = &m->plans.back();
-    }
-    PersistArgs pa;
-    pa.phases = pe->phases;
-    pa.streams = reinterpret_cast<const PersistStream *>(pe->phases + pe->n);
-    pa.nphases = pe->n;
-    pa.bar = m->pbar;
-    pa.err = m->err;
-    pa.part = m->ppart;
-    pa.rg_ticket = m->pticket;
-    CK(launch_decode_persistent(pa, m->cfg.weight_dtype == BLOOM_WEIGHT_INT8, m->pgrid, s));
-    return BLOOM_OK;
 }
 
 extern "C" bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
@@ -925,15 +746,14 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
     if (kv->len < 1) return fail(BLOOM_E_INVALID, "decode before prefill");
     if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full (%d slots)", kv->max_seq);
     cudaStream_t s = (cudaStream_t)stream;
-    if (use_persistent(m, kv->batch)) {
-        if ((st = decode_persistent(m, kv, next_tokens, out_tokens, out_logits, s))) return st;
-    } else if (m->cfg.flags & BLOOM_FLAG_NO_GRAPH) {
+    if (m->cfg.flags & BLOOM_FLAG_NO_GRAPH) {
         CK(enqueue_decode(m, kv, next_tokens, out_tokens, out_logits, s));
     } else {
         cudaGraphExec_t exec = nullptr;
         for (auto &g : m->graphs)
-            if (g.kvbuf == kv->buf && g.next == next_tokens && g.out == out_tokens &&
-                g.logits == out_logits && g.B == kv->batch) {
+            if (g.kvbuf == kv->buf && g.kvbytes == kv->bytes && g.B == kv->batch &&
+                g.max_seq == kv->max_seq && g.next == next_tokens && g.out == out_tokens &&
+                g.logits == out_logits) {
                 exec = g.exec;
                 break;
             }
@@ -954,10 +774,54 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
                 cudaGraphExecDestroy(m->graphs.front().exec);
                 m->graphs.erase(m->graphs.begin());
             }
-            m->graphs.push_back({kv->buf, next_tokens, out_tokens, out_logits, kv->batch, exec});
+            m->graphs.push_back({kv->buf, kv->bytes, kv->batch, kv->max_seq, next_tokens,
+                                 out_tokens, out_logits, exec});
         }
         CK(cudaGraphLaunch(exec, s));
     }
+    kv->len += 1;
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_decode_profile(bloom_model *m, bloom_kv *kv,
+                                             const int32_t *next_tokens, int32_t *out_tokens,
+                                             int32_t *codes, float *ms, int32_t cap, int32_t *n,
+                                             void *stream) {
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!next_tokens || !out_tokens || !codes || !ms || !n || cap < 1)
+        return fail(BLOOM_E_INVALID, "null or empty argument");
+    if (kv->len < 1) return fail(BLOOM_E_INVALID, "decode before prefill");
+    if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full (%d slots)", kv->max_seq);
+    *n = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    g_pdl = false;   // each launch starts after the previous one has finished
+    LaunchProfile prof;
+    cudaEvent_t start = nullptr;
+    CK(cudaEventCreate(&start));
+    cudaError_t e = cudaEventRecord(start, s);
+    if (e == cudaSuccess) {
+        g_prof = &prof;
+        e = enqueue_decode(m, kv, next_tokens, out_tokens, nullptr, s);
+        g_prof = nullptr;
+    }
+    if (e == cudaSuccess) e = prof.err;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaEvent_t prev = start;
+    for (size_t i = 0; i < prof.ev.size(); ++i) {
+        float t = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, prev, prof.ev[i]);
+        if ((int32_t)i < cap) {
+            codes[i] = prof.code[i];
+            ms[i] = t;
+        }
+        prev = prof.ev[i];
+    }
+    for (cudaEvent_t ev : prof.ev) cudaEventDestroy(ev);
+    cudaEventDestroy(start);
+    g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
+    CK(e);
+    *n = (int32_t)std::min<size_t>(prof.ev.size(), (size_t)cap);
     kv->len += 1;
     return BLOOM_OK;
 }
@@ -1065,9 +929,7 @@ extern "C" bloom_status bloom_lm_head(bloom_model *m, const void *xn, int32_t B,
         TcMap mx;
         if (!gemm_make_map(mx.b, xn, B, m->cfg.hidden, nt))
             return fail(BLOOM_E_UNSUPPORTED, "TMA descriptor of xn could not be encoded");
-        GemvTcArgs g;
-        g.a = a;
-        CK(launch_gemv_tc(m->head_wmap.b, mx.b, g, nt, (cudaStream_t)stream));
+        CK(launch_gemv_tc(m->head_wmap.b, mx.b, tc_args(m, a), nt, (cudaStream_t)stream));
         return BLOOM_OK;
     }
     CK(launch_linear(a, m->num_sms, (cudaStream_t)stream));
@@ -1185,19 +1047,8 @@ extern "C" bloom_status bloom_op_linear_tc(const bloom_linear *lin, const void *
     GemvTcArgs g;
     g.a = lin_args(*lin, 0, (const uint16_t *)x, M, N, K, epilogue);
     g.a.out = (uint16_t *)y;
-    g.splits = gemv_tc_splits(N, K, sms, epilogue);
-    void *scratch = nullptr;
-    if (g.splits > 1) {
-        const size_t pb = align256(gemv_tc_part_floats(N, K, M, sms) * 4);
-        const size_t bytes = pb + (size_t)((N + 127) / 128) * 4;
-        CK(cudaMallocAsync(&scratch, bytes, s));
-        CK(cudaMemsetAsync((char *)scratch + pb, 0, bytes - pb, s));
-        g.part = (float *)scratch;
-        g.ticket = (int *)((char *)scratch + pb);
-    }
-    cudaError_t e = launch_gemv_tc(mw.b, mx.b, g, nt, s);
-    if (scratch) cudaFreeAsync(scratch, s);
-    CK(e);
+    g.splits = gemv_tc_splits(N, K, M, epilogue, sms);
+    CK(launch_gemv_tc(mw.b, mx.b, g, nt, s));
     return BLOOM_OK;
 }
 

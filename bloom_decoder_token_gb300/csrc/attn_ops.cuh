@@ -1,6 +1,5 @@
 // Split-KV decode attention for one (sequence, head, key range), as a device
-// function of a whole thread block: used by the per-launch decode attention
-// kernel and by the persistent decode kernel.
+// function of a whole thread block (the body of the decode attention kernel).
 //
 // Score of key k for a query of head j:  s_k = (q . k_k) / sqrt(d) + slope_j * pos_k,
 // where pos_k is the key's position counted from the sequence's first token;

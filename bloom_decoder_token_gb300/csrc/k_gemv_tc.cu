@@ -2,12 +2,10 @@
 //
 // y[m][n] = epilogue(sum_k x[m][k] W[n][k]) for the B tokens of a decode step
 // (B up to 256).  At decode the time is the time to stream W once ("DeepSpeed
-// Inference", III.A); the weight-streaming mma.sync kernel does that well for
-// one or two tokens, but from 8 tokens on its registers and shared-memory
-// traffic per weight byte grow with B.  Here W is the MMA's A operand (128
-// weight rows per tile) and the step's tokens are its N operand (NT = B rounded
-// up to 16, 32, 64, 128 or 256 columns), so the tensor cores take any batch at
-// no extra cost per weight byte:
+// Inference", III.A).  W is the MMA's A operand (128 weight rows per tile)
+// and the step's tokens are its N operand (NT = B rounded up to 16, 32, 64,
+// 128 or 256 columns), so the tensor cores take any batch at no extra cost
+// per weight byte:
 //  * warp 0, one lane: TMA producer.  Each stage holds a 128 x 64 weight tile
 //    and the NT x 64 activation tile of the same k (2-D tensor maps, 128-byte
 //    swizzle).  The weight tiles of the first stages are requested before the
@@ -19,17 +17,24 @@
 //    columns per tcgen05.ld: bias, GeLU, float32 residual add, the Q/K/V
 //    scatter into the cache slot of the step, or the LM head's logits and
 //    argmax (the fusions of "DeepSpeed Inference", III.D).
-// In the decode step this kernel runs the tied LM head (the largest single
-// weight stream: V x h) for 8 or more sequences, where it streams at twice the
-// weight-streaming kernel's rate (2 GB head of the 7b1 shape, 32 sequences:
-// 334 us vs 675 us), and the bf16 block linears from 8 sequences on where
-// they are wide or long (7b1 shape, 32 sequences: up 26 us vs 49 us).
-// Narrow matrices split K over several CTAs so that the grid fills the GPU;
-// each split stores its float32 partial tile and the last split of a row tile
-// to finish (a ticket, no waiting) sums the partials in split order, so the
-// result does not depend on timing.  Every mbarrier wait is bounded (about two
-// seconds of SM clock); on expiry the kernel records kErrTimeout, skips its
-// stores and still frees TMEM.
+//
+// The grid is (row tiles) x (K splits), two CTAs per SM (about 100 KB of
+// weights in flight each).  A matrix with few row tiles (4096 rows = 32 tiles)
+// would leave most SMs idle, so K is split S ways (gemv_tc_splits).  The S
+// splits of a row tile run as one thread-block cluster: each token group of 4
+// is finished by one CTA of the cluster, every split pushes its float32
+// partial of that group into the finisher's shared memory (distributed shared
+// memory stores, no waiting on loads), and after a cluster barrier each CTA
+// sums what it received in split order -- the result does not depend on
+// timing, and no global scratch or second pass is needed (the cross-CTA
+// reduction of SBI-GeMM, "DeepSpeed Inference", III.C.2, kept on chip).  The
+// residuals a finisher adds are loaded during the main loop.
+//
+// Every mbarrier wait is bounded (about two seconds of SM clock); on expiry
+// the kernel records kErrTimeout, skips its stores and still frees TMEM.  The
+// two cluster barriers are reached on every path (every wait before them is
+// bounded), so no CTA of a cluster waits on a peer that has left, and no CTA
+// writes into a peer's shared memory after that peer has passed the second.
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ops.cuh"
@@ -42,7 +47,8 @@ constexpr int kGvBK = 64;                         // k per stage: one 128-byte s
 constexpr int kGvThreads = 192;                   // 6 warps
 constexpr int kGvWBytes = kGvRows * kGvBK * 2;    // 16 KB
 constexpr int kGvSmemBudget = 108 * 1024;         // two CTAs per SM
-constexpr int kGvTargetCtas = 120;                // CTAs a K split aims for
+constexpr int kGvMaxSplits = 16;                  // largest cluster (non-portable size)
+constexpr int kGvMinKbPerSplit = 4;               // k-blocks a split streams at least
 
 template <int NT>
 struct GvCfg {
@@ -52,44 +58,92 @@ struct GvCfg {
     static constexpr int Stages = StagesFit > 8 ? 8 : (StagesFit < 2 ? 2 : StagesFit);
     static constexpr size_t Smem = (size_t)Stages * Stage + 1024;   // + alignment slack
     static constexpr int TmemCols = NT < 32 ? 32 : NT;
+    // K split: the receive area of pushed partials, [split][128 rows][groups
+    // this CTA finishes] float4 (4 tokens), lives in the idle ring; at most
+    // NT / 4 + kGvMaxSplits float4 per row
+    static constexpr bool CanSplit =
+        (size_t)(NT / 4 + kGvMaxSplits) * kGvRows * 16 <= (size_t)Stages * Stage;
 };
 
-__device__ __forceinline__ void epi_bar_sync() {   // the four epilogue warps only
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+// ---- cluster helpers (distributed shared memory)
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_dsmem4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
 }
 
-// Epilogue of one (row n, token m) value.
-template <int EPI>
-__device__ __forceinline__ void gv_apply(const LinearArgs &a, int m, int n, float v, float bias,
-                                         int slot, unsigned long long &best) {
-    v += bias;
-    const size_t o = (size_t)m * a.N + n;
-    if constexpr (EPI == EPI_STORE) {
-        a.out[o] = f2bf(v);
-    } else if constexpr (EPI == EPI_GELU) {
-        a.out[o] = f2bf(gelu_tanh(v));
-    } else if constexpr (EPI == EPI_RESID) {
-        a.out[o] = f2bf(bf2f(a.out[o]) + v);
-    } else if constexpr (EPI == EPI_RESID32) {
-        a.out32[o] += v;
-    } else if constexpr (EPI == EPI_QKV) {
-        const int dh = a.head_dim;
-        const int hj = n / (3 * dh);
-        const int cidx = (n / dh) % 3;
-        const int e = n % dh;
-        if (cidx == 0) {
-            a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e] = f2bf(v);
-        } else if (slot >= 0 && slot < a.max_seq) {
-            uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
-            cache[(((size_t)m * a.n_head + hj) * a.max_seq + slot) * dh + e] = f2bf(v);
-        } else if (a.err) {
-            atomicOr(a.err, kErrSlot);
+// Epilogue of J consecutive tokens m0.. of one row n (v: accumulators, the
+// bias not yet added).  The residual epilogues take the residual values in
+// `res` when the caller loaded them ahead (during the main loop), else every
+// load is issued before any store, so the J tokens cost one memory round trip.
+template <int EPI, int J>
+__device__ __forceinline__ void gv_apply(const LinearArgs &a, int m0, int mmax, int n, const float *v,
+                                         float bias, int slot, unsigned long long *best,
+                                         const float *res = nullptr) {
+    if constexpr (EPI == EPI_RESID32 || EPI == EPI_RESID) {
+        float r[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            if (res) {
+                r[j] = res[j];
+            } else if (m0 + j < mmax) {
+                if constexpr (EPI == EPI_RESID32) r[j] = a.out32[(size_t)(m0 + j) * a.N + n];
+                else r[j] = bf2f(a.out[(size_t)(m0 + j) * a.N + n]);
+            } else {
+                r[j] = 0.f;
+            }
         }
-    } else if constexpr (EPI == EPI_ARGMAX) {
-        if (a.logits) a.logits[o] = v;
-        best = pack_argmax(v, (uint32_t)n);
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            if (m0 + j >= mmax) break;
+            if constexpr (EPI == EPI_RESID32) a.out32[(size_t)(m0 + j) * a.N + n] = r[j] + (v[j] + bias);
+            else a.out[(size_t)(m0 + j) * a.N + n] = f2bf(r[j] + (v[j] + bias));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int m = m0 + j;
+            if (m >= mmax) break;
+            const float x = v[j] + bias;
+            const size_t o = (size_t)m * a.N + n;
+            if constexpr (EPI == EPI_STORE) {
+                a.out[o] = f2bf(x);
+            } else if constexpr (EPI == EPI_GELU) {
+                a.out[o] = f2bf(gelu_tanh(x));
+            } else if constexpr (EPI == EPI_QKV) {
+                const int dh = a.head_dim;
+                const int hj = n / (3 * dh);
+                const int cidx = (n / dh) % 3;
+                const int e = n % dh;
+                if (cidx == 0) {
+                    a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e] = f2bf(x);
+                } else if (slot >= 0 && slot < a.max_seq) {
+                    uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
+                    cache[(((size_t)m * a.n_head + hj) * a.max_seq + slot) * dh + e] = f2bf(x);
+                } else if (a.err) {
+                    atomicOr(a.err, kErrSlot);
+                }
+            } else if constexpr (EPI == EPI_ARGMAX) {
+                if (a.logits) a.logits[o] = x;
+                best[j] = pack_argmax(x, (uint32_t)n);
+            }
+        }
     }
 }
+
+// Token groups (4 tokens) whose residuals a CTA of a K split loads ahead.
+constexpr int kGvResGroups = 4;
 
 template <int EPI, int NT>
 __global__ void __launch_bounds__(kGvThreads, 1)
@@ -101,12 +155,12 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         ((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t full[C::Stages], empty[C::Stages], acc_full;
     __shared__ uint32_t tmem_base;
-    __shared__ int s_abort, s_last_tile, s_last;
+    __shared__ int s_abort, s_last;
     __shared__ unsigned long long s_best[EPI == EPI_ARGMAX ? kMaxBatch : 1];
 
     const LinearArgs &a = g.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x, split = blockIdx.y;
+    const int tile = blockIdx.x, split = blockIdx.y;   // the cluster spans the splits
     const int n0 = tile * kGvRows;
     const int nkb = (a.K + kGvBK - 1) / kGvBK;
     const int per = (nkb + g.splits - 1) / g.splits;
@@ -174,7 +228,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 tc_tma_2d(st + kGvWBytes, &tm_x, (kb0 + i) * kGvBK, 0, &full[s]);
                 ++issued;
             }
-            // no copy of ours may still be landing when the CTA exits
+            // no copy of ours may still be landing when the stages are reused or
+            // the CTA exits
             for (int j = 0; j < C::Stages && j < issued; ++j) {
                 const int i = issued - 1 - j;
                 if (!tc_mbar_wait(&full[i % C::Stages], (uint32_t)((i / C::Stages) & 1)) && a.err)
@@ -207,72 +262,144 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             }
             tc_commit(&acc_full);   // accumulator complete (or abandoned)
         }
-    } else {
-        // ---- epilogue: warps 2..5 -> TMEM lane quarters (warp % 4); thread = weight row
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;
-        const int n = n0 + r;
-        const bool nok = n < a.N;
+    }
+    __syncwarp();
+
+    // ---- epilogue: warps 2..5 -> TMEM lane quarters (warp % 4); thread = weight row
+    const bool epi_warp = warp >= 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int n = n0 + r;
+    const bool nok = n < a.N;
+    const int mmax = a.M < NT ? a.M : NT;
+    const int S = g.splits;
+    const int groups = (mmax + 3) / 4;
+    float bias = 0.f;
+    int slot = 0;
+    bool live = false;
+    // residuals of the token groups this CTA finishes (split, split + S, ...),
+    // loaded while the main loop runs
+    constexpr bool kRes = (EPI == EPI_RESID32 || EPI == EPI_RESID) && C::CanSplit;
+    float res[kRes ? 4 * kGvResGroups : 1];
+    if (epi_warp) {
         griddep_wait();   // the residual and the cache belong to earlier kernels too
-        const float bias = (a.bias && nok) ? bf2f(a.bias[n]) : 0.f;
-        const int slot = (EPI == EPI_QKV && a.len_ptr) ? *a.len_ptr : 0;
+        bias = (a.bias && nok) ? bf2f(a.bias[n]) : 0.f;
+        slot = (EPI == EPI_QKV && a.len_ptr) ? *a.len_ptr : 0;
+        if constexpr (kRes) {
+            if (S > 1) {
+#pragma unroll
+                for (int q = 0; q < kGvResGroups; ++q)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int m = (split + q * S) * 4 + j;
+                        float v = 0.f;
+                        if (nok && m < mmax) {
+                            if constexpr (EPI == EPI_RESID32) v = a.out32[(size_t)m * a.N + n];
+                            else v = bf2f(a.out[(size_t)m * a.N + n]);
+                        }
+                        res[4 * q + j] = v;
+                    }
+            }
+        }
         // longer limit than the MMA issuer's, so that its final commit arrives first
         const bool ok = tc_mbar_wait(&acc_full, 0, 3 * kTcWaitCycles);
         if (!ok && a.err) atomicOr(a.err, kErrTimeout);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         // warp-uniform, so that the argmax shuffles below see every lane
-        const bool live = __all_sync(0xffffffffu, ok && !*(volatile int *)&s_abort);
-        const int mmax = a.M < NT ? a.M : NT;
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-        if (g.splits == 1) {
+        live = __all_sync(0xffffffffu, ok && !*(volatile int *)&s_abort);
+    }
+    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+    if (S == 1) {
+        if (epi_warp) {
 #pragma unroll 1
             for (int c = 0; c < NT; c += 16) {
                 float v[16];
                 tc_ld16(taddr + (uint32_t)c, v);   // whole warp
-                if (!live) continue;               // warp-uniform
+                if (!live || c >= mmax) continue;  // warp-uniform
+                if (!my_kb) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int m = c + j;
-                    if (m >= mmax) break;          // warp-uniform
-                    unsigned long long best = 0;   // rows past N take no part
-                    if (nok) gv_apply<EPI>(a, m, n, my_kb ? v[j] : 0.f, bias, slot, best);
-                    if constexpr (EPI == EPI_ARGMAX) {
-                        // max over the warp's 32 rows (every lane shuffles), then the CTA's
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                }
+                unsigned long long best[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) best[j] = 0;   // rows past N take no part
+                if (nok) gv_apply<EPI, 16>(a, c, mmax, n, v, bias, slot, best);
+                if constexpr (EPI == EPI_ARGMAX) {
+                    // max over the warp's 32 rows (every lane shuffles), then the CTA's
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        unsigned long long b = best[j];
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) {
-                            const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
-                            best = ob > best ? ob : best;
+                            const unsigned long long ob = __shfl_xor_sync(0xffffffffu, b, o);
+                            b = ob > b ? ob : b;
                         }
-                        if (lane == 0 && best) atomicMax(&s_best[m], best);
+                        if (lane == 0 && b && c + j < mmax) atomicMax(&s_best[c + j], b);
                     }
                 }
             }
-        } else {
-            // split K: store this split's partial tile [NT][128], the last split sums
-            float *mine = g.part + ((size_t)tile * g.splits + split) * NT * kGvRows;
+        }
+    } else if constexpr (C::CanSplit && EPI != EPI_ARGMAX) {
+        // K split over the cluster.  Token group gi (4 tokens) is finished by the
+        // CTA of rank gi % S; every split pushes its partial of that group into
+        // the finisher's receive area [split][128 rows][gpc] (float4), in the
+        // finisher's ring, which is idle once every split is past its main loop
+        // (all its MMAs have completed and every copy into it has landed).
+        const int gpc = (groups + S - 1) / S;
+        float4 *recv = reinterpret_cast<float4 *>(smem);
+        __syncwarp();
+        cluster_arrive();   // this CTA's ring is idle
+        cluster_wait();     // ... and every peer's
+        if (epi_warp) {
+            const uint32_t rb = tc_smem(recv);
+            const bool use = live && my_kb > 0;
 #pragma unroll 1
             for (int c = 0; c < NT; c += 16) {
                 float v[16];
-                tc_ld16(taddr + (uint32_t)c, v);
+                tc_ld16(taddr + (uint32_t)c, v);   // whole warp
+                if (c >= mmax) continue;           // warp-uniform
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c + j < mmax) mine[(size_t)(c + j) * kGvRows + r] = (live && my_kb) ? v[j] : 0.f;
-            }
-            __threadfence();
-            epi_bar_sync();
-            if (tid == 64) s_last_tile = (atomicAdd(g.ticket + tile, 1) == g.splits - 1);
-            epi_bar_sync();
-            if (s_last_tile) {
-                __threadfence();
-                const float *base = g.part + (size_t)tile * g.splits * NT * kGvRows;
-                for (int m = 0; m < mmax; ++m) {
-                    float t = 0.f;
-                    for (int sp = 0; sp < g.splits; ++sp)
-                        t += __ldcg(base + ((size_t)sp * NT + m) * kGvRows + r);
-                    unsigned long long best = 0;
-                    if (live && nok) gv_apply<EPI>(a, m, n, t, bias, slot, best);
+                for (int q = 0; q < 4; ++q) {
+                    const int gi = c / 4 + q;
+                    if (gi >= groups) break;
+                    const float4 val = use ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3])
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const uint32_t off = (uint32_t)(((split * kGvRows + r) * gpc + gi / S) * 16);
+                    st_dsmem4(dsmem_map(rb + off, (uint32_t)(gi % S)), val);
                 }
-                if (tid == 64) g.ticket[tile] = 0;
+            }
+        }
+        __syncwarp();
+        cluster_arrive();   // every push has landed once all have arrived
+        cluster_wait();
+        if (epi_warp && nok && !*(volatile int *)&s_abort) {
+            // sum of group lg's S partials, in split order
+            auto gsum = [&](int lg, float (&t)[4]) {
+                t[0] = t[1] = t[2] = t[3] = 0.f;
+                for (int sp = 0; sp < S; ++sp) {
+                    const float4 p = recv[(sp * kGvRows + r) * gpc + lg];
+                    t[0] += p.x;
+                    t[1] += p.y;
+                    t[2] += p.z;
+                    t[3] += p.w;
+                }
+            };
+#pragma unroll
+            for (int lg = 0; lg < kGvResGroups; ++lg) {   // residuals loaded ahead
+                const int gi = lg * S + split;
+                if (lg < gpc && gi < groups) {
+                    float t[4];
+                    gsum(lg, t);
+                    gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, slot, nullptr,
+                                     kRes ? res + 4 * lg : nullptr);
+                }
+            }
+            for (int lg = kGvResGroups; lg < gpc; ++lg) {
+                const int gi = lg * S + split;
+                if (gi >= groups) break;
+                float t[4];
+                gsum(lg, t);
+                gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, slot, nullptr);
             }
         }
     }
@@ -295,47 +422,67 @@ int gemv_tc_nt(int M) {
     return M <= 256 ? 256 : 0;
 }
 
-// K splits per row tile: the fewest that fill the GPU's CTA slots (two CTAs
-// per SM) in whole waves, at most one split per 4 k-blocks.
-// K splits of a launch: enough CTAs for about kGvTargetCtas SMs and no more.
-// Measured on GB300 at 16-64 tokens, an unsplit 96- or 128-tile matrix streams
-// at 65-79 % of the copy peak while 2-7 splits of it (more CTAs, each partial
-// tile written, and summed by the last split) ran at 27-55 %; a 32-tile matrix
-// wants 4.
-int gemv_tc_splits(int N, int K, int num_sms, int epi) {
-    (void)num_sms;
-    if (epi == EPI_ARGMAX) return 1;
+int gemv_tc_box_rows_w() { return kGvRows; }
+
+// K splits of a launch: the fewest that give at least 1.5 CTAs per SM, while
+// all CTAs still fit at once (two per SM) and every split streams >= 4
+// k-blocks.  Measured per matrix on GB300 (7b1 shapes, 1-32 tokens, launches
+// back to back): QKV (96 row tiles) is fastest split 3 ways, the MLP up
+// (128 tiles) 2 ways, the 4096-row dense and down (32 tiles) 8 ways; unsplit,
+// those leave 24-120 SMs idle (QKV 23 vs 21 us, down 75 vs 28 us).
+int gemv_tc_splits(int N, int K, int M, int epi, int num_sms) {
+    const int nt = gemv_tc_nt(M);
+    if (epi == EPI_ARGMAX || nt == 0 || nt == 256 || num_sms < 1) return 1;
     const int tiles = (N + kGvRows - 1) / kGvRows;
     const int nkb = (K + kGvBK - 1) / kGvBK;
-    int s = (kGvTargetCtas + tiles / 2) / tiles;   // rounded: 96 or 128 tiles -> 1, 32 -> 4
-    if (s > 16) s = 16;
-    while (s > 1 && s * 4 > nkb) --s;   // at least 4 k-blocks per split
-    return s < 1 ? 1 : s;
+    int s = 1;
+    while (s < kGvMaxSplits && 2 * tiles * s < 3 * num_sms) ++s;        // >= 1.5 CTAs per SM
+    while (s > 1 && (tiles * s > 2 * num_sms || nkb / s < kGvMinKbPerSplit)) --s;
+    return s;
 }
 
-size_t gemv_tc_part_floats(int N, int K, int M, int num_sms) {
-    const int nt = gemv_tc_nt(M);
-    const int tiles = (N + kGvRows - 1) / kGvRows;
-    const int s = gemv_tc_splits(N, K, num_sms, EPI_STORE);
-    return s > 1 ? (size_t)tiles * s * nt * kGvRows : 0;
+template <int EPI, int NT>
+static cudaError_t gv_configure() {
+    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)GvCfg<NT>::Smem);
+    if (e == cudaSuccess && EPI != EPI_ARGMAX && GvCfg<NT>::CanSplit)
+        e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
 }
-
-int gemv_tc_box_rows_w() { return kGvRows; }
 
 template <int EPI, int NT>
 static cudaError_t gv_launch_t(const void *mw, const void *mx, const GemvTcArgs &g, cudaStream_t s) {
     using C = GvCfg<NT>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Smem);
+        cudaError_t e = gv_configure<EPI, NT>();
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    if (g.splits > 1 && (!C::CanSplit || EPI == EPI_ARGMAX)) return cudaErrorInvalidValue;
     const CUtensorMap &tw = *reinterpret_cast<const CUtensorMap *>(mw);
     const CUtensorMap &tx = *reinterpret_cast<const CUtensorMap *>(mx);
-    dim3 grid((g.a.N + kGvRows - 1) / kGvRows, g.splits);
-    return launch_pdl_smem(gemv_tc_kernel<EPI, NT>, grid, dim3(kGvThreads), C::Smem, s, tw, tx, g);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((g.a.N + kGvRows - 1) / kGvRows), (unsigned)g.splits);
+    cfg.blockDim = dim3(kGvThreads);
+    cfg.dynamicSmemBytes = C::Smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+    int na = 1;
+    if (g.splits > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = (unsigned)g.splits;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<EPI, NT>, tw, tx, g);
 }
 
 template <int EPI>
@@ -354,20 +501,11 @@ static cudaError_t gv_launch_epi(const void *mw, const void *mx, const GemvTcArg
 template <int EPI>
 static cudaError_t gv_prepare_epi() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)GvCfg<16>::Smem)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)GvCfg<32>::Smem)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)GvCfg<64>::Smem)))
-        return e;
-    if ((e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)GvCfg<128>::Smem)))
-        return e;
-    return cudaFuncSetAttribute(gemv_tc_kernel<EPI, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)GvCfg<256>::Smem);
+    if ((e = gv_configure<EPI, 16>())) return e;
+    if ((e = gv_configure<EPI, 32>())) return e;
+    if ((e = gv_configure<EPI, 64>())) return e;
+    if ((e = gv_configure<EPI, 128>())) return e;
+    return gv_configure<EPI, 256>();
 }
 
 cudaError_t gemv_tc_prepare() {
@@ -385,7 +523,7 @@ cudaError_t launch_gemv_tc(const void *map_w, const void *map_x, const GemvTcArg
     const LinearArgs &a = g.a;
     if (a.M <= 0 || a.N <= 0) return cudaSuccess;
     if (a.int8 || a.K % 8 || a.T != 0 || gemv_tc_nt(a.M) != nt || a.M > kMaxBatch) return cudaErrorInvalidValue;
-    if (g.splits < 1 || (g.splits > 1 && (!g.part || !g.ticket || a.epi == EPI_ARGMAX)))
+    if (g.splits < 1 || g.splits > kGvMaxSplits || (g.splits > 1 && a.epi == EPI_ARGMAX))
         return cudaErrorInvalidValue;
     switch (a.epi) {
         case EPI_STORE: return gv_launch_epi<EPI_STORE>(map_w, map_x, g, nt, s);

@@ -113,19 +113,14 @@ constexpr int kTcMinM = 128;        // prefill linears with at least this many t
 // Decode linear on the tensor cores (tcgen05 / TMEM / TMA): W is the 128-row
 // A operand, the M <= 256 tokens the N operand (NT = gemv_tc_nt(M) columns).
 // map_w: W [N][K] with box rows gemv_tc_box_rows_w(); map_x: x [>= M][K] with
-// box rows NT.  splits > 1 (K split over CTAs) needs part (gemv_tc_part_floats
-// floats) and ticket (one int per 128-row tile, zero at rest); not for ARGMAX.
+// box rows NT.  splits > 1 splits K over a thread-block cluster of that many
+// CTAs per row tile (gemv_tc_splits; not for ARGMAX or NT = 256).
 struct GemvTcArgs {
     LinearArgs a;
     int splits = 1;
-    float *part = nullptr;
-    int *ticket = nullptr;
 };
-constexpr int kTcDecodeMinM = 8;    // decode steps of at least this many sequences: LM head on it
-constexpr int kTcDecodeBlockMinM = 8;    // ... and the wide or long block linears
 int gemv_tc_nt(int M);
-int gemv_tc_splits(int N, int K, int num_sms, int epi);
-size_t gemv_tc_part_floats(int N, int K, int M, int num_sms);
+int gemv_tc_splits(int N, int K, int M, int epi, int num_sms);
 int gemv_tc_box_rows_w();
 cudaError_t gemv_tc_prepare();
 cudaError_t launch_gemv_tc(const void *map_w, const void *map_x, const GemvTcArgs &g, int nt,
@@ -190,67 +185,5 @@ struct AttnPrefillArgs {
     uint16_t *o = nullptr;           // [B*T][n*d]
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, cudaStream_t s);
-
-// ---- persistent decode step (one cooperative launch per step) ----
-enum PhaseKind : int {
-    PH_EMBED = 0,    // embedding gather + LN of the step's tokens -> float32 rows
-    PH_LN = 1,       // LayerNorm of float32 rows -> bf16 rows
-    PH_LINEAR = 2,   // weight-streaming linear layer (any epilogue; M <= 16)
-    PH_ATTN = 3,     // split-KV decode attention
-};
-
-struct alignas(16) PersistPhase {
-    int kind = PH_LN;
-    // PH_LINEAR: lin.M = batch; tasks = row groups of 8; nchunks = 64-byte chunks
-    // per row (32 bf16 or 64 int8 k each); nbt = 4-chunk batches per row group;
-    // tb = tasks * nbt, the phase's batches, split into one piece per warp
-    LinearArgs lin;
-    int tasks = 0, nchunks = 0, nbt = 0;
-    long long tb = 0;
-    int xs = 0;                         // activations staged in shared memory for the phase
-    // PH_LN / PH_EMBED
-    int rows = 0, h = 0;
-    float eps = 1e-5f;
-    const uint16_t *g = nullptr, *b = nullptr;
-    const float *ln_src = nullptr;      // LN: float [rows][h]
-    uint16_t *ln_dst = nullptr;         // LN: bf16 [rows][h]
-    const int *tokens = nullptr;        // EMBED: token per row
-    const uint16_t *emb = nullptr;      // EMBED: bf16 [vocab][h]
-    int vocab = 0;
-    float *emb_dst = nullptr;           // EMBED: float [rows][h]
-    const int *len = nullptr, *next_pos = nullptr;   // EMBED: pos[r][*len] = next_pos[r]
-    int *pos = nullptr;
-    int max_seq = 0;
-    // PH_ATTN: units = B * n * splits, one per thread-block visit
-    AttnDecodeArgs at;
-};
-
-// A phase's weight stream as the persistent kernel walks it (tb = 0: no weights).
-struct PersistStream {
-    const char *w = nullptr;
-    long long tb = 0;
-    int nbt = 0, N = 0, row_bytes = 0, pad = 0;
-};
-
-struct PersistArgs {
-    const PersistPhase *phases = nullptr;
-    const PersistStream *streams = nullptr;   // one per phase
-    int nphases = 0;
-    unsigned *bar = nullptr;   // [0] barrier arrivals, [1] exit ticket, [2] abort; zero at rest
-    int *err = nullptr;
-    float *part = nullptr;     // [grid * 8 warps][2][128] partial tiles of shared row groups
-    int *rg_ticket = nullptr;  // [largest row-group count of any phase], zero at rest
-};
-
-constexpr int kPersistMaxM = 16;    // batch rows the persistent step takes (one mma token tile)
-// Chunk geometry of a linear phase as the persistent kernel streams it.
-void persist_linear_geometry(PersistPhase &ph);
-cudaError_t persist_prepare();
-// Whether the device can hold one persistent block on every SM; the grid size.
-int persist_grid(int int8);
-size_t persist_part_bytes(int grid);
-int persist_max_phases(int int8);       // phases whose stream table fits in shared memory
-size_t persist_smem_bytes(int nphases);
-cudaError_t launch_decode_persistent(const PersistArgs &pa, int int8, int grid, cudaStream_t s);
 
 }  // namespace bloom

@@ -63,14 +63,10 @@ enum {
                                  waits for the previous one to finish before it starts) */
     BLOOM_FLAG_NO_LN_FUSION = 4, /* run every LayerNorm as its own kernel instead of inside
                                     the decode linear kernel that consumes it */
-    BLOOM_FLAG_NO_TC_GEMM = 8,   /* every linear on the weight-streaming kernel instead of the
+    BLOOM_FLAG_NO_TC_GEMM = 8    /* every linear on the weight-streaming kernel instead of the
                                     tensor-core (tcgen05) kernels: the prefill GEMM (>= 128
                                     tokens), the decode LM head (>= 8 sequences) and the wide
                                     or long bf16 decode block linears (>= 8 sequences) */
-    BLOOM_FLAG_PERSISTENT = 16   /* decode steps of <= 16 sequences as one persistent
-                                    cooperative launch (all layers as phases separated by grid
-                                    barriers) instead of one launch per operation replayed as a
-                                    CUDA graph */
 };
 
 typedef struct {
@@ -171,6 +167,40 @@ bloom_status bloom_generate(bloom_model *m, bloom_kv *kv, const int32_t *tokens_
                             const uint8_t *mask_host, int32_t B, int32_t T, int32_t n_new,
                             int32_t *out_host, void *stream);
 
+/* Operations and kernels of a decode step, as bloom_decode_profile reports
+ * them: code = op | (kernel << 8). */
+enum {
+    BLOOM_OP_EMBED = 0,       /* embedding gather + embedding LayerNorm */
+    BLOOM_OP_LAYERNORM = 1,   /* LN1 / LN2 / ln_f as a kernel of its own */
+    BLOOM_OP_QKV = 2,         /* fused QKV + bias + K/V append */
+    BLOOM_OP_ATTN = 3,        /* ALiBi attention over the cache */
+    BLOOM_OP_DENSE = 4,       /* attention output projection + bias + residual */
+    BLOOM_OP_UP = 5,          /* MLP up projection + bias + GeLU */
+    BLOOM_OP_DOWN = 6,        /* MLP down projection + bias + residual */
+    BLOOM_OP_HEAD = 7         /* tied LM head + argmax */
+};
+enum {
+    BLOOM_KERNEL_EMBED = 0,
+    BLOOM_KERNEL_LAYERNORM = 1,
+    BLOOM_KERNEL_STREAM = 2,          /* weight-streaming mma.sync linear */
+    BLOOM_KERNEL_GEMV_TC = 3,         /* tensor-core (tcgen05) decode linear */
+    BLOOM_KERNEL_GEMM_TC = 4,         /* tensor-core (tcgen05) prefill GEMM */
+    BLOOM_KERNEL_ATTN = 5,            /* split-KV decode attention */
+    BLOOM_KERNEL_ATTN_PREFILL = 6     /* prefill attention */
+};
+
+/* One decode step exactly as bloom_decode_step computes it (same kernels,
+ * same results, kv->len advanced), but launched one kernel at a time, each
+ * starting after the previous one has finished, with a CUDA event recorded
+ * on `stream` after every launch; for measuring the share of each kernel in a
+ * step.  Fills codes[i] (op | kernel << 8) and ms[i] (the launch's duration,
+ * from the previous event) for the first min(cap, launches) launches, sets *n
+ * to that count, and synchronises the stream.  codes, ms and n are HOST
+ * pointers.  Not for use inside a stream capture. */
+bloom_status bloom_decode_profile(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
+                                  int32_t *out_tokens, int32_t *codes, float *ms, int32_t cap,
+                                  int32_t *n, void *stream);
+
 /* Synchronise the stream, read and clear the device flag: BLOOM_OK or
  * BLOOM_E_DEVICE_FLAG (the flag's bits are in bloom_last_error()). */
 bloom_status bloom_check_device(bloom_model *m, void *stream);
@@ -182,7 +212,7 @@ bloom_status bloom_destroy(bloom_model *m);
 const char *bloom_last_error(void);
 
 /* Kernel launches one decode step of `batch` sequences issues (for launch
- * accounting): 1 for the persistent step, else one per operation. */
+ * accounting): one per operation, less the LayerNorms fused into a linear. */
 int32_t bloom_decode_launches(const bloom_model *m, int32_t batch);
 
 /* ------------------------------------------------------------------------

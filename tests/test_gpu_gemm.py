@@ -172,7 +172,8 @@ def test_linear_tc(M, N, K, epi):
 
 
 def test_linear_tc_deterministic_split_k():
-    """K split over CTAs: partials summed in split order, so repeated runs agree bitwise."""
+    """K split over a thread-block cluster: partials summed in split order, so
+    repeated runs agree bitwise."""
     g = gen(77)
     W = bf((512, 16384), g, 0.02).to(DEV)
     x = bf((24, 16384), g).to(DEV)
@@ -192,9 +193,10 @@ def test_decode_generation_batch16(flags):
 @pytest.mark.parametrize("flags", [0, bg.FLAG_NO_TC_GEMM], ids=["tcgen05", "streaming"])
 def test_decode_block_linears_through_tcgen05(B, flags):
     """An 8192-wide MLP (up: N = 8192, down: K = 8192) at 8, 16 and 32 sequences:
-    the decode step runs those two linears on the tensor-core decode kernel
-    (down with its K split summed by the last split), against the oracle, and
-    against the weight-streaming path for the same inputs."""
+    the decode step runs the block linears on the tensor-core decode kernel
+    (K split over a cluster, partials summed through distributed shared
+    memory), against the oracle, and against the weight-streaming path for the
+    same inputs."""
     shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=4096, ffn=8192, batch=B, prompt=8,
                                         ragged=True)
     w = synth.make_weights(shape, seed=21, random_affine=True)
@@ -203,10 +205,42 @@ def test_decode_block_linears_through_tcgen05(B, flags):
 
 def test_decode_qkv_through_tcgen05():
     """A 2816-wide stack with 22 heads of 128 at 8 sequences: the decode QKV
-    linear (8448 rows) runs on the tensor-core decode kernel with its K split in
-    two, the Q/K/V scatter into the cache applied by the last split; up (11264
-    rows) unsplit; down (K = 11264) split five ways.  Against the oracle."""
+    linear (8448 rows) runs on the tensor-core decode kernel with its K split
+    over a cluster, the Q/K/V scatter into the cache applied by the CTA that
+    sums each token group.  Against the oracle."""
     shape = synth.PRESETS["560m"].with_(n_layer=1, hidden=2816, n_head=22, ffn=11264,
                                         vocab=4096, batch=8, prompt=8, ragged=True)
     w = synth.make_weights(shape, seed=23, random_affine=True)
     generate_parity(shape, w, steps=2, tol=2e-2)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_decode_small_batch_through_tcgen05(B):
+    """One to three sequences: dense and down (and from three sequences QKV, up
+    and the head) on the tensor-core decode kernel, QKV / up / head on the
+    weight-streaming kernel with the LayerNorm fused at one and two."""
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000, batch=B, prompt=8, ragged=True)
+    w = synth.make_weights(shape, seed=31 + B, random_affine=True)
+    generate_parity(shape, w, steps=3, tol=2e-2)
+
+
+# The 176B-layer matrices at full size (QKV 43008 x 14336, up 57344 x 14336,
+# down 14336 x 57344) on the tensor-core decode kernel, compared with the oracle
+# on 384 sampled output rows (the oracle computes those rows directly).
+@pytest.mark.slow
+@pytest.mark.parametrize("N,K", [(43008, 14336), (57344, 14336), (14336, 57344)],
+                         ids=["qkv", "up", "down"])
+@pytest.mark.parametrize("M", [8, 32, 256])
+def test_linear_tc_176b_shapes_sampled(N, K, M):
+    g = torch.Generator(device=DEV).manual_seed(N + K + M)
+    W = (0.02 * torch.randn(N, K, generator=g, device=DEV)).to(torch.bfloat16)
+    x = torch.randn(M, K, generator=g, device=DEV).to(torch.bfloat16)
+    bias = (0.5 * torch.randn(N, generator=g, device=DEV)).to(torch.bfloat16)
+    y = bg.op_linear_tc(x, W, bias=bias, epilogue=bg.EPI_GELU)
+    rows = torch.randperm(N, generator=torch.Generator().manual_seed(M))[:384].sort().values
+    Ws = W[rows.to(DEV)].cpu()
+    acc = oracle.linear(f64(x), oracle.host_bits(Ws), oracle.host_bits(bias[rows.to(DEV)].cpu()))
+    ref = np.vectorize(oracle.gelu)(acc)
+    assert_kernel_close(y[:, rows.to(DEV)], ref, what=f"linear_tc {M}x{N}x{K} sampled rows")
+    del W
+    torch.cuda.empty_cache()

@@ -100,11 +100,70 @@ def test_560m_shape_generation():
     generate_parity(shape, w, steps=3, tol=2e-2)
 
 
-@pytest.mark.parametrize("flags", [0, bg.FLAG_PERSISTENT], ids=["per_launch", "persistent"])
+@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_GRAPH], ids=["graph", "no_graph"])
 def test_560m_shape_random_affine_two_layers(flags):
     shape = synth.PRESETS["560m"].with_(n_layer=2)
     w = synth.make_weights(shape, seed=1, random_affine=True)
     generate_parity(shape, w, steps=4, tol=2e-2, flags=flags)
+
+
+def test_reinit_cache_buffer_with_smaller_max_seq():
+    """A decode graph bakes in the cache layout (max_seq sets every stride):
+    re-binding the same buffer with the same batch and a smaller max_seq must
+    not replay the old graph.  Both bindings decode against the oracle."""
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=4000)
+    w = synth.make_weights(shape, seed=6, random_affine=True)
+    ids, mask = synth.make_prompts(shape, seed=6)
+    B, T = ids.shape
+    gm = bg.Model(w.to(DEV), max_batch=B, max_tokens=B * T, max_seq=T + 8)
+    om = oracle.Model(w)
+    kv = gm.new_kv(B, T + 8)
+    nxt_d = torch.empty(B, dtype=torch.int32, device=DEV)
+    lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
+    for max_seq in (T + 8, T + 3):
+        # same buffer, new layout
+        bg.check(bg.lib().bloom_kv_init(gm.h, bg.C.byref(kv.c), bg.P(kv.view.data_ptr()),
+                                        kv.view.numel(), B, max_seq, None))
+        seqs = om.new_seqs(B, max_seq)
+        gm.prefill(kv, ids.to(DEV), mask.to(DEV), logits=lg)
+        ref = om.prefill(seqs, ids.numpy(), mask.numpy())
+        for _ in range(2):
+            nxt = torch.from_numpy(ref.argmax(axis=1).astype(np.int32))
+            nxt_d.copy_(nxt)
+            gm.decode_step(kv, nxt_d, nxt_d, logits=lg)
+            ref = om.decode(seqs, nxt.numpy())
+            assert max_abs(lg, ref) <= 2e-2, max_seq
+    gm.check_device()
+    gm.close()
+
+
+def test_decode_profile_matches_decode_step():
+    """The launch-by-launch profile step computes the same tokens and cache as
+    a graph-replayed step and reports one entry per launch of the step."""
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000)
+    w = synth.make_weights(shape, seed=7, random_affine=True).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=7)
+    B, T = ids.shape
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=T + 4)
+    outs = []
+    for profiled in (False, True):
+        kv = gm.new_kv(B, T + 4)
+        tok = gm.prefill(kv, ids.to(DEV), mask.to(DEV))
+        for _ in range(2):
+            if profiled:
+                rows = gm.decode_profile(kv, tok, tok)
+                assert len(rows) == gm.decode_launches(B)
+                assert [r[0] for r in rows][0] == "embed" and rows[-1][0] == "head"
+                assert all(r[2] > 0 for r in rows)
+            else:
+                gm.decode_step(kv, tok, tok)
+        torch.cuda.synchronize()
+        # slots written so far (the rest of each buffer was never initialised)
+        outs.append((tok.cpu(), kv.tensors(gm)["k"][:, :, :, :kv.len].cpu(), kv.len))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert outs[0][2] == outs[1][2]
+    gm.close()
 
 
 def test_graph_replay_equals_direct_launches():
