@@ -88,7 +88,7 @@ _SIGS = {
     "bloom_op_layernorm": (I32, [P, P, P, I32, I32, C.c_float, P, P]),
     "bloom_op_linear": (I32, [C.POINTER(Linear), I32, P, I32, I32, I32, I32, P, P]),
     "bloom_op_gemm": (I32, [C.POINTER(Linear), P, I32, I32, I32, I32, P, P]),
-    "bloom_op_linear_tc": (I32, [C.POINTER(Linear), P, I32, I32, I32, I32, P, P]),
+    "bloom_op_linear_tc": (I32, [C.POINTER(Linear), I32, P, I32, I32, I32, I32, P, P]),
     "bloom_op_attn_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P]),
     "bloom_op_lmhead_argmax": (I32, [P, P, I32, I32, I32, P, P, P]),
     "bloom_op_lmhead_argmax_noalloc": (I32, [P, P, I32, I32, I32, P, P, P]),
@@ -318,15 +318,17 @@ def op_gemm(x, w, bias=None, epilogue=EPI_STORE, y=None, stream=None):
     return y
 
 
-def op_linear_tc(x, w, bias=None, epilogue=EPI_STORE, y=None, stream=None):
-    """bf16 linear layer on the tensor-core decode kernel (M <= 256 tokens)."""
+def op_linear_tc(x, w=None, bias=None, q=None, scale=None, epilogue=EPI_STORE, y=None,
+                 stream=None):
+    """Linear layer on the tensor-core decode kernel: bf16 weights w (M <= 256
+    tokens) or int8 codes q with bf16 row scales (M <= 128)."""
     M, K = x.shape
-    N = w.shape[0]
+    N = (w if w is not None else q).shape[0]
     if y is None:
         y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
-    lin = Linear(_p(w), None, _p(bias))
-    check(lib().bloom_op_linear_tc(C.byref(lin), _p(x), M, N, K, epilogue, _p(y),
-                                   _stream(stream)))
+    lin = Linear(_p(w if w is not None else q), _p(scale), _p(bias))
+    check(lib().bloom_op_linear_tc(C.byref(lin), 0 if w is not None else 1, _p(x), M, N, K,
+                                   epilogue, _p(y), _stream(stream)))
     return y
 
 

@@ -296,7 +296,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         else
             m->tcd = true;
     }
-    if (!st2 && m->tcd && !i8) {
+    if (!st2 && m->tcd) {
         const int F = cfg->ffn;
         const int ntmax = gemv_tc_nt(cfg->max_batch);
         bool ok = true;
@@ -305,10 +305,9 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
         for (int l = 0; ok && l < cfg->n_layer; ++l) {
             const bloom_layer_weights &L = w->layers[l];
             TcMap *wm = &m->dwmaps[(size_t)l * TC_PER_LAYER];
-            ok = gemm_make_map(wm[TC_QKV].b, L.qkv.w, 3 * h, h, bw) &&
-                 gemm_make_map(wm[TC_O].b, L.o.w, h, h, bw) &&
-                 gemm_make_map(wm[TC_UP].b, L.up.w, F, h, bw) &&
-                 gemm_make_map(wm[TC_DOWN].b, L.down.w, h, F, bw);
+            auto mk = i8 ? gemm_make_map_u8 : gemm_make_map;
+            ok = mk(wm[TC_QKV].b, L.qkv.w, 3 * h, h, bw) && mk(wm[TC_O].b, L.o.w, h, h, bw) &&
+                 mk(wm[TC_UP].b, L.up.w, F, h, bw) && mk(wm[TC_DOWN].b, L.down.w, h, F, bw);
         }
         for (int ci = 0; ok && ci < kTcNtClasses && (16 << ci) <= ntmax; ++ci)
             ok = gemm_make_map(m->dxmaps[TC_X_A][ci].b, m->a, cfg->max_batch, h, 16 << ci) &&
@@ -477,7 +476,7 @@ static void prof_mark(cudaStream_t s, int op, int kernel) {
 static GemvTcArgs tc_args(const bloom_model *m, const LinearArgs &a) {
     GemvTcArgs g;
     g.a = a;
-    g.splits = gemv_tc_splits(a.N, a.K, a.M, a.epi, m->num_sms);
+    g.splits = gemv_tc_splits(a.N, a.K, a.M, a.epi, m->num_sms, a.int8);
     return g;
 }
 
@@ -499,8 +498,8 @@ static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t
 // the 7b1 step at one sequence took 4.17 ms instead of 3.18.
 constexpr int kTcBlockMinM = 3;
 static bool use_tc_linear(const bloom_model *m, const LinearArgs &a) {
-    return m->tcb && a.T == 0 && !a.int8 && !a.ln_x && a.M >= kTcBlockMinM &&
-           a.M <= m->cfg.max_batch && !prefers_ln_fusion(m, a);
+    return m->tcb && a.T == 0 && !a.ln_x && a.M >= kTcBlockMinM && a.M <= m->cfg.max_batch &&
+           (!a.int8 || a.M <= kGvInt8MaxNt) && !prefers_ln_fusion(m, a);
 }
 
 // A linear layer of decoder layer l: the tensor-core GEMM for prefill batches of
@@ -1022,15 +1021,16 @@ extern "C" bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, in
     return BLOOM_OK;
 }
 
-extern "C" bloom_status bloom_op_linear_tc(const bloom_linear *lin, const void *x, int32_t M,
-                                           int32_t N, int32_t K, int32_t epilogue, void *y,
-                                           void *stream) {
+extern "C" bloom_status bloom_op_linear_tc(const bloom_linear *lin, int32_t int8, const void *x,
+                                           int32_t M, int32_t N, int32_t K, int32_t epilogue,
+                                           void *y, void *stream) {
     g_pdl = true;
     if (!lin) return fail(BLOOM_E_INVALID, "null argument");
-    bloom_status st = check_linear(*lin, 0, N, K, "op", -1);
+    bloom_status st = check_linear(*lin, int8, N, K, "op", -1);
     if (st) return st;
     if (M < 0 || N < 1) return fail(BLOOM_E_INVALID, "M=%d N=%d", M, N);
-    if (M > kMaxBatch) return fail(BLOOM_E_CAPACITY, "M=%d above %d", M, kMaxBatch);
+    if (M > (int8 ? kGvInt8MaxNt : kMaxBatch))
+        return fail(BLOOM_E_CAPACITY, "M=%d above %d", M, int8 ? kGvInt8MaxNt : kMaxBatch);
     if (epilogue < BLOOM_EPI_STORE || epilogue > BLOOM_EPI_RESID)
         return fail(BLOOM_E_INVALID, "epilogue %d", epilogue);
     if (M == 0) return BLOOM_OK;
@@ -1040,14 +1040,14 @@ extern "C" bloom_status bloom_op_linear_tc(const bloom_linear *lin, const void *
     const int nt = gemv_tc_nt(M);
     TcMap mx, mw;
     if (gemm_map_bytes() != sizeof(TcMap) || !gemm_make_map(mx.b, x, M, K, nt) ||
-        !gemm_make_map(mw.b, lin->w, N, K, gemv_tc_box_rows_w()))
+        !(int8 ? gemm_make_map_u8 : gemm_make_map)(mw.b, lin->w, N, K, gemv_tc_box_rows_w()))
         return fail(BLOOM_E_UNSUPPORTED, "TMA descriptors could not be encoded");
     CK(gemv_tc_prepare());
     cudaStream_t s = (cudaStream_t)stream;
     GemvTcArgs g;
-    g.a = lin_args(*lin, 0, (const uint16_t *)x, M, N, K, epilogue);
+    g.a = lin_args(*lin, int8, (const uint16_t *)x, M, N, K, epilogue);
     g.a.out = (uint16_t *)y;
-    g.splits = gemv_tc_splits(N, K, M, epilogue, sms);
+    g.splits = gemv_tc_splits(N, K, M, epilogue, sms, int8);
     CK(launch_gemv_tc(mw.b, mx.b, g, nt, s));
     return BLOOM_OK;
 }

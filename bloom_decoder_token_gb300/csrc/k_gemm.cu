@@ -332,6 +332,21 @@ bool gemm_make_map(void *map, const void *base, long long rows, long long K, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D uint8 tensor map over rows x K bytes (row-major int8 weights), boxes of
+// box_rows x 128 bytes, 128B swizzle.
+bool gemm_make_map_u8(void *map, const void *base, long long rows, long long K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || ((uintptr_t)base & 15u) || K % 16) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t gemm_map_bytes() { return sizeof(CUtensorMap); }
 int gemm_box_rows_x() { return kTcBM; }
 int gemm_box_rows_w() { return kTcBN; }

@@ -50,14 +50,20 @@ constexpr int kGvSmemBudget = 108 * 1024;         // two CTAs per SM
 constexpr int kGvMaxSplits = 16;                  // largest cluster (non-portable size)
 constexpr int kGvMinKbPerSplit = 4;               // k-blocks a split streams at least
 
-template <int NT>
+// W8: int8 weights.  A stage then holds a 128 x 128 int8 weight tile (the same
+// 16 KB) and the NT x 128 activations (two 64-wide boxes); the epilogue warps
+// widen each stage's codes into one of two TMEM A buffers (64 columns of bf16
+// pairs each, columns [0, 128)), the accumulator sits at column 128.
+template <int NT, bool W8 = false>
 struct GvCfg {
-    static constexpr int XBytes = NT * kGvBK * 2;
+    static constexpr int KB = W8 ? 128 : kGvBK;   // k per stage
+    static constexpr int XBytes = NT * KB * 2;
     static constexpr int Stage = kGvWBytes + XBytes;
     static constexpr int StagesFit = kGvSmemBudget / Stage;
     static constexpr int Stages = StagesFit > 8 ? 8 : (StagesFit < 2 ? 2 : StagesFit);
     static constexpr size_t Smem = (size_t)Stages * Stage + 1024;   // + alignment slack
-    static constexpr int TmemCols = NT < 32 ? 32 : NT;
+    static constexpr int TmemCols = W8 ? 256 : (NT < 32 ? 32 : NT);
+    static constexpr uint32_t AccCol = W8 ? 128u : 0u;
     // K split: the receive area of pushed partials, [split][128 rows][groups
     // this CTA finishes] float4 (4 tokens), lives in the idle ring; at most
     // NT / 4 + kGvMaxSplits float4 per row
@@ -145,15 +151,16 @@ __device__ __forceinline__ void gv_apply(const LinearArgs &a, int m0, int mmax, 
 // Token groups (4 tokens) whose residuals a CTA of a K split loads ahead.
 constexpr int kGvResGroups = 4;
 
-template <int EPI, int NT>
+template <int EPI, int NT, bool W8>
 __global__ void __launch_bounds__(kGvThreads, 1)
 gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                const GemvTcArgs g) {
-    using C = GvCfg<NT>;
+    using C = GvCfg<NT, W8>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         ((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t full[C::Stages], empty[C::Stages], acc_full;
+    __shared__ uint64_t a_full[W8 ? 2 : 1], a_empty[W8 ? 2 : 1];   // TMEM A buffers (W8)
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort, s_last;
     __shared__ unsigned long long s_best[EPI == EPI_ARGMAX ? kMaxBatch : 1];
@@ -162,7 +169,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, split = blockIdx.y;   // the cluster spans the splits
     const int n0 = tile * kGvRows;
-    const int nkb = (a.K + kGvBK - 1) / kGvBK;
+    const int nkb = (a.K + C::KB - 1) / C::KB;
     const int per = (nkb + g.splits - 1) / g.splits;
     const int kb0 = split * per;
     const int kb1 = min(nkb, kb0 + per);
@@ -174,6 +181,12 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             tc_mbar_init(&empty[s], 1);
         }
         tc_mbar_init(&acc_full, 1);
+        if constexpr (W8) {
+            for (int b = 0; b < 2; ++b) {
+                tc_mbar_init(&a_full[b], 4);    // one arrival per converting warp
+                tc_mbar_init(&a_empty[b], 1);   // the MMA issuer's commit
+            }
+        }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_w) : "memory");
@@ -198,6 +211,12 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         if (lane == 0) {
             // ---- TMA producer.  Weight tiles of the first stages go out before the
             // wait for the previous kernel (they do not depend on it).
+            auto load_x = [&](unsigned char *st, int i, uint64_t *bar) {
+#pragma unroll
+                for (int h = 0; h < C::KB / kGvBK; ++h)
+                    tc_tma_2d(st + kGvWBytes + h * NT * 128, &tm_x, (kb0 + i) * C::KB + h * kGvBK, 0,
+                              bar);
+            };
             const int pre = my_kb < C::Stages ? my_kb : C::Stages;
             for (int i = 0; i < pre; ++i) {
                 unsigned char *st = smem + (size_t)i * C::Stage;
@@ -205,12 +224,10 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                                  tc_smem(&full[i])),
                              "r"(C::Stage)
                              : "memory");
-                tc_tma_2d(st, &tm_w, (kb0 + i) * kGvBK, n0, &full[i]);
+                tc_tma_2d(st, &tm_w, (kb0 + i) * C::KB, n0, &full[i]);
             }
             griddep_wait();   // the activations come from the previous kernel
-            for (int i = 0; i < pre; ++i)
-                tc_tma_2d(smem + (size_t)i * C::Stage + kGvWBytes, &tm_x, (kb0 + i) * kGvBK, 0,
-                          &full[i]);
+            for (int i = 0; i < pre; ++i) load_x(smem + (size_t)i * C::Stage, i, &full[i]);
             int issued = pre;
             for (int i = pre; i < my_kb; ++i) {
                 const int s = i % C::Stages;
@@ -224,8 +241,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                                  tc_smem(&full[s])),
                              "r"(C::Stage)
                              : "memory");
-                tc_tma_2d(st, &tm_w, (kb0 + i) * kGvBK, n0, &full[s]);
-                tc_tma_2d(st + kGvWBytes, &tm_x, (kb0 + i) * kGvBK, 0, &full[s]);
+                tc_tma_2d(st, &tm_w, (kb0 + i) * C::KB, n0, &full[s]);
+                load_x(st, i, &full[s]);
                 ++issued;
             }
             // no copy of ours may still be landing when the stages are reused or
@@ -240,6 +257,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         if (lane == 0) {
             // ---- MMA issuer
             constexpr uint32_t idesc = tc_idesc(kGvRows, NT);
+            const uint32_t acc = tmem + C::AccCol;
             bool ok = true;
             for (int i = 0; i < my_kb; ++i) {
                 const int s = i % C::Stages;
@@ -247,14 +265,31 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     ok = false;
                     break;
                 }
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t sw = tc_smem(smem + (size_t)s * C::Stage);
-                const uint64_t dw = tc_desc(sw), dx = tc_desc(sw + kGvWBytes);
+                if constexpr (W8) {
+                    // the widened weights of this stage, in TMEM A buffer i % 2
+                    if (!tc_mbar_wait(&a_full[i & 1], (uint32_t)((i >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t ta = tmem + (uint32_t)((i & 1) * 64);
 #pragma unroll
-                for (int k = 0; k < kGvBK / 16; ++k)   // 16 bf16 = 32 bytes per step
-                    tc_mma(tmem, dw + (uint64_t)(2 * k), dx + (uint64_t)(2 * k), idesc,
-                           (i > 0 || k > 0) ? 1u : 0u);
-                tc_commit(&empty[s]);
+                    for (int k = 0; k < C::KB / 16; ++k) {   // 8 steps of 16: two activation boxes
+                        const uint64_t dx = tc_desc(sw + kGvWBytes + (k / 4) * NT * 128) + (uint64_t)(2 * (k % 4));
+                        tc_mma_tmem_a(acc, ta + (uint32_t)(8 * k), dx, idesc, (i > 0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);
+                    tc_commit(&a_empty[i & 1]);
+                } else {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint64_t dw = tc_desc(sw), dx = tc_desc(sw + kGvWBytes);
+#pragma unroll
+                    for (int k = 0; k < kGvBK / 16; ++k)   // 16 bf16 = 32 bytes per step
+                        tc_mma(acc, dw + (uint64_t)(2 * k), dx + (uint64_t)(2 * k), idesc,
+                               (i > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(&empty[s]);
+                }
             }
             if (!ok) {
                 s_abort = 1;
@@ -281,7 +316,50 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     // loaded while the main loop runs
     constexpr bool kRes = (EPI == EPI_RESID32 || EPI == EPI_RESID) && C::CanSplit;
     float res[kRes ? 4 * kGvResGroups : 1];
+    const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
+    float scale = 1.f;
     if (epi_warp) {
+        if constexpr (W8) {
+            // widen this thread's weight row of every stage (128 int8 codes, exact in
+            // bf16) into TMEM A buffer i % 2 for the MMA issuer
+            for (int i = 0; i < my_kb; ++i) {
+                const int s = i % C::Stages;
+                const bool wok = __all_sync(
+                    0xffffffffu, tc_mbar_wait(&full[s], (uint32_t)((i / C::Stages) & 1)) &&
+                                     (i < 2 || tc_mbar_wait(&a_empty[i & 1], (uint32_t)(((i >> 1) - 1) & 1))));
+                if (!wok) {   // warp-uniform
+                    s_abort = 1;
+                    if (a.err) atomicOr(a.err, kErrTimeout);
+                    break;
+                }
+                const unsigned char *wrow = smem + (size_t)s * C::Stage + (size_t)r * 128;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int c = hh * 4 + cc;   // 16-byte chunk, swizzled by the row
+                        const uint4 q = *reinterpret_cast<const uint4 *>(wrow + ((c ^ (r & 7)) << 4));
+                        w[cc * 8 + 0] = i8x2_to_bf16x2(q.x, 0);
+                        w[cc * 8 + 1] = i8x2_to_bf16x2(q.x, 2);
+                        w[cc * 8 + 2] = i8x2_to_bf16x2(q.y, 0);
+                        w[cc * 8 + 3] = i8x2_to_bf16x2(q.y, 2);
+                        w[cc * 8 + 4] = i8x2_to_bf16x2(q.z, 0);
+                        w[cc * 8 + 5] = i8x2_to_bf16x2(q.z, 2);
+                        w[cc * 8 + 6] = i8x2_to_bf16x2(q.w, 0);
+                        w[cc * 8 + 7] = i8x2_to_bf16x2(q.w, 2);
+                    }
+                    tc_st32(tlane + (uint32_t)((i & 1) * 64 + hh * 32), w);
+                }
+                tc_wait_st();
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0)
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem(&a_full[i & 1]))
+                                 : "memory");
+            }
+            scale = nok ? bf2f(a.scale[n]) : 0.f;
+        }
         griddep_wait();   // the residual and the cache belong to earlier kernels too
         bias = (a.bias && nok) ? bf2f(a.bias[n]) : 0.f;
         slot = (EPI == EPI_QKV && a.len_ptr) ? *a.len_ptr : 0;
@@ -308,7 +386,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         // warp-uniform, so that the argmax shuffles below see every lane
         live = __all_sync(0xffffffffu, ok && !*(volatile int *)&s_abort);
     }
-    const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t taddr = tlane + C::AccCol;
     if (S == 1) {
         if (epi_warp) {
 #pragma unroll 1
@@ -316,10 +394,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 float v[16];
                 tc_ld16(taddr + (uint32_t)c, v);   // whole warp
                 if (!live || c >= mmax) continue;  // warp-uniform
-                if (!my_kb) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                }
+                for (int j = 0; j < 16; ++j) v[j] = my_kb ? v[j] * scale : 0.f;
                 unsigned long long best[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) best[j] = 0;   // rows past N take no part
@@ -390,6 +466,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 if (lg < gpc && gi < groups) {
                     float t[4];
                     gsum(lg, t);
+                    for (int j = 0; j < 4; ++j) t[j] *= scale;
                     gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, slot, nullptr,
                                      kRes ? res + 4 * lg : nullptr);
                 }
@@ -399,6 +476,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 if (gi >= groups) break;
                 float t[4];
                 gsum(lg, t);
+                for (int j = 0; j < 4; ++j) t[j] *= scale;
                 gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, slot, nullptr);
             }
         }
@@ -430,34 +508,35 @@ int gemv_tc_box_rows_w() { return kGvRows; }
 // back to back): QKV (96 row tiles) is fastest split 3 ways, the MLP up
 // (128 tiles) 2 ways, the 4096-row dense and down (32 tiles) 8 ways; unsplit,
 // those leave 24-120 SMs idle (QKV 23 vs 21 us, down 75 vs 28 us).
-int gemv_tc_splits(int N, int K, int M, int epi, int num_sms) {
+int gemv_tc_splits(int N, int K, int M, int epi, int num_sms, int int8) {
     const int nt = gemv_tc_nt(M);
     if (epi == EPI_ARGMAX || nt == 0 || nt == 256 || num_sms < 1) return 1;
     const int tiles = (N + kGvRows - 1) / kGvRows;
-    const int nkb = (K + kGvBK - 1) / kGvBK;
+    const int kb = int8 ? 128 : kGvBK;   // k per stage
+    const int nkb = (K + kb - 1) / kb;
     int s = 1;
     while (s < kGvMaxSplits && 2 * tiles * s < 3 * num_sms) ++s;        // >= 1.5 CTAs per SM
     while (s > 1 && (tiles * s > 2 * num_sms || nkb / s < kGvMinKbPerSplit)) --s;
     return s;
 }
 
-template <int EPI, int NT>
+template <int EPI, int NT, bool W8>
 static cudaError_t gv_configure() {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)GvCfg<NT>::Smem);
-    if (e == cudaSuccess && EPI != EPI_ARGMAX && GvCfg<NT>::CanSplit)
-        e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT>,
+    using C = GvCfg<NT, W8>;
+    cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT, W8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::Smem);
+    if (e == cudaSuccess && EPI != EPI_ARGMAX && C::CanSplit)
+        e = cudaFuncSetAttribute(gemv_tc_kernel<EPI, NT, W8>,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
 }
 
-template <int EPI, int NT>
+template <int EPI, int NT, bool W8>
 static cudaError_t gv_launch_t(const void *mw, const void *mx, const GemvTcArgs &g, cudaStream_t s) {
-    using C = GvCfg<NT>;
+    using C = GvCfg<NT, W8>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = gv_configure<EPI, NT>();
+        cudaError_t e = gv_configure<EPI, NT, W8>();
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -482,18 +561,29 @@ static cudaError_t gv_launch_t(const void *mw, const void *mx, const GemvTcArgs 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<EPI, NT>, tw, tx, g);
+    return cudaLaunchKernelEx(&cfg, gemv_tc_kernel<EPI, NT, W8>, tw, tx, g);
 }
 
 template <int EPI>
 static cudaError_t gv_launch_epi(const void *mw, const void *mx, const GemvTcArgs &g, int nt,
                                  cudaStream_t s) {
+    if constexpr (EPI != EPI_ARGMAX) {
+        if (g.a.int8) {
+            switch (nt) {   // int8 weights: up to 128 token columns (TMEM A buffers + accumulator)
+                case 16: return gv_launch_t<EPI, 16, true>(mw, mx, g, s);
+                case 32: return gv_launch_t<EPI, 32, true>(mw, mx, g, s);
+                case 64: return gv_launch_t<EPI, 64, true>(mw, mx, g, s);
+                case 128: return gv_launch_t<EPI, 128, true>(mw, mx, g, s);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+    }
     switch (nt) {
-        case 16: return gv_launch_t<EPI, 16>(mw, mx, g, s);
-        case 32: return gv_launch_t<EPI, 32>(mw, mx, g, s);
-        case 64: return gv_launch_t<EPI, 64>(mw, mx, g, s);
-        case 128: return gv_launch_t<EPI, 128>(mw, mx, g, s);
-        case 256: return gv_launch_t<EPI, 256>(mw, mx, g, s);
+        case 16: return gv_launch_t<EPI, 16, false>(mw, mx, g, s);
+        case 32: return gv_launch_t<EPI, 32, false>(mw, mx, g, s);
+        case 64: return gv_launch_t<EPI, 64, false>(mw, mx, g, s);
+        case 128: return gv_launch_t<EPI, 128, false>(mw, mx, g, s);
+        case 256: return gv_launch_t<EPI, 256, false>(mw, mx, g, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -501,11 +591,18 @@ static cudaError_t gv_launch_epi(const void *mw, const void *mx, const GemvTcArg
 template <int EPI>
 static cudaError_t gv_prepare_epi() {
     cudaError_t e;
-    if ((e = gv_configure<EPI, 16>())) return e;
-    if ((e = gv_configure<EPI, 32>())) return e;
-    if ((e = gv_configure<EPI, 64>())) return e;
-    if ((e = gv_configure<EPI, 128>())) return e;
-    return gv_configure<EPI, 256>();
+    if ((e = gv_configure<EPI, 16, false>())) return e;
+    if ((e = gv_configure<EPI, 32, false>())) return e;
+    if ((e = gv_configure<EPI, 64, false>())) return e;
+    if ((e = gv_configure<EPI, 128, false>())) return e;
+    if ((e = gv_configure<EPI, 256, false>())) return e;
+    if constexpr (EPI != EPI_ARGMAX) {   // the LM head is always bf16
+        if ((e = gv_configure<EPI, 16, true>())) return e;
+        if ((e = gv_configure<EPI, 32, true>())) return e;
+        if ((e = gv_configure<EPI, 64, true>())) return e;
+        if ((e = gv_configure<EPI, 128, true>())) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t gemv_tc_prepare() {
@@ -522,7 +619,9 @@ cudaError_t launch_gemv_tc(const void *map_w, const void *map_x, const GemvTcArg
                            cudaStream_t s) {
     const LinearArgs &a = g.a;
     if (a.M <= 0 || a.N <= 0) return cudaSuccess;
-    if (a.int8 || a.K % 8 || a.T != 0 || gemv_tc_nt(a.M) != nt || a.M > kMaxBatch) return cudaErrorInvalidValue;
+    if (a.T != 0 || gemv_tc_nt(a.M) != nt || a.M > kMaxBatch) return cudaErrorInvalidValue;
+    if (a.int8 ? (a.K % 16 || !a.scale || nt > kGvInt8MaxNt || a.epi == EPI_ARGMAX) : a.K % 8)
+        return cudaErrorInvalidValue;
     if (g.splits < 1 || g.splits > kGvMaxSplits || (g.splits > 1 && a.epi == EPI_ARGMAX))
         return cudaErrorInvalidValue;
     switch (a.epi) {

@@ -101,6 +101,8 @@ cudaError_t launch_linear(const LinearArgs &a, int num_sms, cudaStream_t s);
 // returns false if the driver refuses (base not 16-byte aligned, K % 8 != 0).
 // X maps use box rows gemm_box_rows_x(), W maps gemm_box_rows_w().
 bool gemm_make_map(void *map, const void *base, long long rows, long long K, int box_rows);
+// The same for int8 weights [rows][K] (K % 16 == 0): boxes of box_rows x 128 bytes.
+bool gemm_make_map_u8(void *map, const void *base, long long rows, long long K, int box_rows);
 size_t gemm_map_bytes();
 int gemm_box_rows_x();
 int gemm_box_rows_w();
@@ -112,15 +114,17 @@ constexpr int kTcMinM = 128;        // prefill linears with at least this many t
 
 // Decode linear on the tensor cores (tcgen05 / TMEM / TMA): W is the 128-row
 // A operand, the M <= 256 tokens the N operand (NT = gemv_tc_nt(M) columns).
-// map_w: W [N][K] with box rows gemv_tc_box_rows_w(); map_x: x [>= M][K] with
-// box rows NT.  splits > 1 splits K over a thread-block cluster of that many
+// map_w: W [N][K] with box rows gemv_tc_box_rows_w() (gemm_make_map, or
+// gemm_make_map_u8 for int8 weights: a.int8, a.scale, M <= 128, not ARGMAX);
+// map_x: x [>= M][K] with box rows NT.  splits > 1 splits K over a thread-block cluster of that many
 // CTAs per row tile (gemv_tc_splits; not for ARGMAX or NT = 256).
 struct GemvTcArgs {
     LinearArgs a;
     int splits = 1;
 };
 int gemv_tc_nt(int M);
-int gemv_tc_splits(int N, int K, int M, int epi, int num_sms);
+int gemv_tc_splits(int N, int K, int M, int epi, int num_sms, int int8 = 0);
+constexpr int kGvInt8MaxNt = 128;   // int8 weights: token columns up to this
 int gemv_tc_box_rows_w();
 cudaError_t gemv_tc_prepare();
 cudaError_t launch_gemv_tc(const void *map_w, const void *map_x, const GemvTcArgs &g, int nt,

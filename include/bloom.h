@@ -288,16 +288,18 @@ bloom_status bloom_op_linear(const bloom_linear *lin, int32_t int8, const void *
 bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, int32_t M, int32_t N,
                            int32_t K, int32_t epilogue, void *y, void *stream);
 
-/* The same linear layer on the tensor-core decode kernel (the LM head of
- * decode steps of 8 or more sequences runs on it): W is the 128-row operand of
- * tcgen05.mma, the M <= 256
- * tokens its N operand, both moved by TMA, the accumulator in TMEM; narrow
- * matrices split K over several CTAs and the last split sums the partials in
- * split order ("DeepSpeed Inference", III.A: small-batch cost is reading W).
- * bf16 weights only; x and lin->w 16-byte aligned; K % 8 == 0.  Same
- * epilogues and result layout as bloom_op_linear. */
-bloom_status bloom_op_linear_tc(const bloom_linear *lin, const void *x, int32_t M, int32_t N,
-                                int32_t K, int32_t epilogue, void *y, void *stream);
+/* The same linear layer on the tensor-core decode kernel (the decode steps of
+ * 3 or more sequences run their linears on it): W is the 128-row operand of
+ * tcgen05.mma, the tokens its N operand, both moved by TMA, the accumulator in
+ * TMEM; narrow matrices split K over a thread-block cluster whose partials are
+ * summed in split order ("DeepSpeed Inference", III.A: small-batch cost is
+ * reading W).  int8 = 0: bf16 weights, M <= 256, K % 8 == 0.  int8 = 1: int8
+ * codes with bf16 row scales (lin->scale), widened exactly to bf16 on the chip
+ * and scaled per row in the epilogue, M <= 128, K % 16 == 0 ("Incredibly Fast
+ * BLOOM Inference...", Key observations: int8 halves the bytes read).  x and
+ * lin->w 16-byte aligned.  Same epilogues and result layout as bloom_op_linear. */
+bloom_status bloom_op_linear_tc(const bloom_linear *lin, int32_t int8, const void *x, int32_t M,
+                                int32_t N, int32_t K, int32_t epilogue, void *y, void *stream);
 
 /* Split-KV decode attention for one token per sequence.
  * q bf16 [B][n][d]; k_cache, v_cache bf16 [B][n][max_seq][d]; pos int32

@@ -109,6 +109,11 @@ def test_ops_reject_bad_arguments(lib):
     lin = bg.Linear(C.c_void_p(16), None, None)
     assert lib.bloom_op_linear(C.byref(lin), 0, C.c_void_p(16), 1, 4, 12, 0, C.c_void_p(16), None) == 2
     assert lib.bloom_op_linear(C.byref(lin), 0, C.c_void_p(16), 1, 4, 16, 9, C.c_void_p(16), None) == 1
+    lin8 = bg.Linear(C.c_void_p(16), C.c_void_p(16), None)
+    assert lib.bloom_op_linear_tc(C.byref(lin8), 1, C.c_void_p(16), 129, 128, 64, 0,
+                                  C.c_void_p(16), None) == 4      # int8: at most 128 tokens
+    assert lib.bloom_op_linear_tc(C.byref(lin8), 1, C.c_void_p(16), 8, 128, 72, 0,
+                                  C.c_void_p(16), None) == 2      # int8 rows in 16-byte chunks
     assert lib.bloom_decode_step(None, None, None, None, None, None) == 1
     assert lib.bloom_destroy(None) == 0
 

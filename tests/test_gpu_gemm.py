@@ -244,3 +244,64 @@ def test_linear_tc_176b_shapes_sampled(N, K, M):
     assert_kernel_close(y[:, rows.to(DEV)], ref, what=f"linear_tc {M}x{N}x{K} sampled rows")
     del W
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- int8 on the tensor-core decode kernel
+# int8 codes are widened exactly to bf16 into a TMEM A operand; ragged N, a K
+# tail that is not a multiple of the 128-wide int8 k-block, split and unsplit.
+INT8_TC_SHAPES = [(3, 300, 192), (8, 3072, 1024), (17, 520, 1040), (32, 4096, 4096),
+                  (64, 1040, 2048), (100, 256, 16384), (128, 12288, 4096), (33, 128, 64)]
+
+
+@pytest.mark.parametrize("M,N,K", INT8_TC_SHAPES)
+@pytest.mark.parametrize("epi", [bg.EPI_STORE, bg.EPI_GELU, bg.EPI_RESID],
+                         ids=["store", "gelu", "resid"])
+def test_linear_tc_int8(M, N, K, epi):
+    g = gen(M * 313 + N * 11 + K + epi)
+    W = bf((N, K), g, 0.02)
+    q, sc = synth.quantize_rows_int8(W)
+    x = bf((M, K), g, 1.0)
+    bias = bf((N,), g, 0.5)
+    y0 = bf((M, N), g, 1.0)
+    acc = oracle.linear(f64(x), q=oracle.host_bits(q), s_bits=oracle.host_bits(sc),
+                        bias_bits=oracle.host_bits(bias))
+    y = y0.to(DEV).clone()
+    bg.op_linear_tc(x.to(DEV), q=q.to(DEV), scale=sc.to(DEV), bias=bias.to(DEV), epilogue=epi, y=y)
+    if epi == bg.EPI_STORE:
+        ref = acc
+    elif epi == bg.EPI_GELU:
+        ref = np.vectorize(oracle.gelu)(acc)
+    else:
+        ref = f64(y0) + acc
+    assert_kernel_close(y, ref, what=f"linear_tc int8 {M}x{N}x{K}")
+
+
+def test_linear_tc_int8_every_code():
+    """Every int8 code (-128 .. 127), at even and odd k, in every 16-byte chunk of
+    the 128-byte swizzled rows and in both 128-wide k-blocks, comes out exactly:
+    with unit scales, no bias and one-hot activations y[m][n] = q[n][p_m].  This
+    pins the widening and the order of the two bf16 values in each TMEM column
+    of the A operand."""
+    N, K = 512, 256
+    n = torch.arange(N).unsqueeze(1)
+    k = torch.arange(K).unsqueeze(0)
+    q = ((3 * n + k) % 256).to(torch.uint8).view(torch.int8)
+    pos = [0, 1, 2, 3, 14, 15, 16, 17, 31, 62, 63, 64, 65, 100, 127, 128, 129, 200, 254, 255]
+    x = torch.zeros(len(pos), K, dtype=torch.bfloat16)
+    for m, p in enumerate(pos):
+        x[m, p] = 1.0
+    scale = torch.ones(N, dtype=torch.bfloat16)
+    y = bg.op_linear_tc(x.to(DEV), q=q.to(DEV), scale=scale.to(DEV))
+    expect = torch.stack([q[:, p].float() for p in pos])
+    assert torch.equal(y.cpu().float(), expect)
+
+
+@pytest.mark.parametrize("B", [3, 8, 32])
+def test_decode_int8_through_tcgen05(B):
+    """int8 block linears of decode steps on the tensor-core decode kernel
+    (QKV, dense, up, down; the head stays bf16), against the oracle at the int8
+    tolerance 6e-2."""
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000, batch=B, prompt=8, ragged=True,
+                                        int8=True)
+    w = synth.make_weights(shape, seed=41 + B, random_affine=True)
+    generate_parity(shape, w, steps=3, tol=6e-2)
