@@ -50,6 +50,16 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s (the burst figure: prefill is timed
+    launch by launch, seconds at most)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 # ------------------------------------------------------------------ byte model
 def linear_shapes(sh: synth.Shape):
     h, F = sh.hidden, sh.ffn
@@ -328,6 +338,56 @@ def decode_series(gm, sh, batches, dev, stream, hbm):
     return out
 
 
+def prefill_flops(sh: synth.Shape, B: int, T: int) -> float:
+    """Algorithmic FLOPs of one prefill of B full prompts of T tokens: the four
+    block linears for every token, causal attention (QK^T and PV over the keys
+    each query sees), and the LM head for the last token of each row."""
+    h, L = sh.hidden, sh.n_layer
+    lin = 2.0 * B * T * sum(N * K for N, K in linear_shapes(sh).values()) * L
+    att = 2.0 * 2.0 * B * L * h * (T * (T + 1) / 2.0)
+    head = 2.0 * B * sh.vocab * h
+    return lin + att + head
+
+
+def prefill_extra(name, B, T, dev, args, bg):
+    """Whole prefill of B prompts of T tokens through bloom_prefill on a preset
+    stack (its own model, freed afterwards): time (CUDA events), TFLOP/s and
+    the fraction of the dense bf16 peak."""
+    sh = synth.PRESETS[name].with_(batch=B, prompt=T, new_tokens=1)
+    w = synth.make_weights(sh, seed=0, device=dev)
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=T + 1, flags=model_flags(args, bg))
+    g = torch.Generator().manual_seed(7)
+    ids = torch.randint(0, sh.vocab, (B, T), generator=g, dtype=torch.int64).to(torch.int32).to(dev)
+    mask = torch.ones(B, T, dtype=torch.uint8, device=dev)
+    kv = gm.new_kv(B, T + 1)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(2):
+        gm.prefill(kv, ids, mask, out_tokens=tok)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(3):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        gm.prefill(kv, ids, mask, out_tokens=tok)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    gm.check_device()
+    gm.close()
+    del gm, w, kv
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    ms = min(times)
+    fl = prefill_flops(sh, B, T)
+    peak, src = bf16_peak()
+    return {"workload": f"{name}: {sh.n_layer} layers, h {sh.hidden}, prefill of {B} x {T} tokens",
+            "prefill_ms": ms, "tflop": fl / 1e12, "tflops": fl / (ms / 1e3) / 1e12,
+            "bf16_peak_tflops": peak, "peak_source": src,
+            "frac_of_bf16_peak": fl / (ms / 1e3) / 1e12 / peak}
+
+
 def kernel_shares(gm, sh, B, T, dev, reps=3):
     """Each operation's share of one decode step, timed launch by launch with
     CUDA events on the step's stream (bloom_decode_profile: the same kernels
@@ -339,7 +399,7 @@ def kernel_shares(gm, sh, B, T, dev, reps=3):
     kv = gm.new_kv(B, T + sh.new_tokens)
     tok = torch.empty(B, dtype=torch.int32, device=dev)
     gm.prefill(kv, ids.to(dev), mask.to(dev), out_tokens=tok)
-    for _ in range(sh.new_tokens // 2 - 1):
+    for _ in range(max(0, min(sh.new_tokens // 2 - 1, sh.new_tokens - 1 - reps))):
         gm.decode_step(kv, tok, tok)
     keys = kv.len + 1
     runs = [gm.decode_profile(kv, tok, tok) for _ in range(reps)]
@@ -486,6 +546,8 @@ def run_ours(args, sh):
         torch.cuda.empty_cache()
         extras["int8_7b1"] = extra_stack("7b1int8", (1, 8, 32, 128), dev, args, bg, hbm)
         extras["cfg_176b14"] = extra_stack("176b14", (1, 8, 32), dev, args, bg, hbm)
+        extras["prefill_176b14_4x2048"] = prefill_extra("176b14", 4, 2048, dev, args, bg)
+        extras["prefill_7b1_128x16"] = prefill_extra("7b1", 128, 16, dev, args, bg)
 
     if rank == 0:
         line = {
@@ -539,6 +601,8 @@ def main():
     ap.add_argument("--cpu-decode-steps", type=int, default=4)
     ap.add_argument("--ref-decode-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", default=None, metavar="PRESET:BxT",
+                    help="only time one whole prefill, e.g. 176b14:4x2048, and print its line")
     ap.add_argument("--no-extras", action="store_true",
                     help="only the workload itself (no batch series, int8 or 176B-shape keys)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
@@ -560,6 +624,13 @@ def main():
         sh = sh.with_(prompt=args.prompt)
     if args.impl == "reference":
         run_reference(args, sh)
+    elif args.prefill_only:
+        import bloom_decoder_token_gb300 as bg
+        name, bt = args.prefill_only.split(":")
+        B, T = (int(v) for v in bt.split("x"))
+        torch.cuda.set_device(0)
+        print(json.dumps({"prefill_only": prefill_extra(name, B, T, torch.device("cuda", 0), args,
+                                                        bg)}), flush=True)
     else:
         run_ours(args, sh)
 

@@ -613,7 +613,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.max_seq = max_seq;
         at.scale = (float)(1.0 / sqrt((double)d));
         at.o = m->o;
-        if ((e = launch_attn_prefill(at, s))) return e;
+        if ((e = launch_attn_prefill_tc(at, s))) return e;
         prof_mark(s, BLOOM_OP_ATTN, BLOOM_KERNEL_ATTN_PREFILL);
     }
     LinearArgs od = lin_args(L.o, i8, m->o, M, h, h, EPI_RESID32);

@@ -188,6 +188,9 @@ struct AttnPrefillArgs {
     float scale = 0.f;
     uint16_t *o = nullptr;           // [B*T][n*d]
 };
-cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, cudaStream_t s);
+// Causal, pad-masked ALiBi attention of every prompt slot on the tensor cores
+// (mma.sync, 64-query x 64-key tiles); d in {64, 128}; rows of q, k and v
+// 16-byte aligned.
+cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs &a, cudaStream_t s);
 
 }  // namespace bloom

@@ -305,3 +305,53 @@ def test_decode_int8_through_tcgen05(B):
                                         int8=True)
     w = synth.make_weights(shape, seed=41 + B, random_affine=True)
     generate_parity(shape, w, steps=3, tol=6e-2)
+
+
+# ---------------------------------------------------------------- prefill attention on tensor cores
+def _prefill_layer_vs_oracle(shape, seed, mask, x_std=1.0, tol=2e-2):
+    """One teacher-forced prefill layer of B prompts of T slots (mask [B][T]):
+    GPU (tcgen05 GEMM + tensor-core attention) against the oracle layer."""
+    w = synth.make_weights(shape.with_(n_layer=1), seed=seed, device=DEV, random_affine=True)
+    B, T = mask.shape
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=T + 1)
+    kv = gm.new_kv(B, T + 1)
+    gm.kv_set_prompt(kv, mask.to(DEV))
+    g = torch.Generator().manual_seed(seed + 100)
+    x_in = (x_std * torch.randn(B * T, shape.hidden, generator=g)).float()
+    xt = x_in.to(DEV)
+    gm.layer_prefill(kv, 0, xt, B, T)
+    om = oracle.Model(synth.Weights(shape, w.word_emb[:1].cpu(), w.emb_ln_g.cpu(), w.emb_ln_b.cpu(),
+                                    w.lnf_g.cpu(), w.lnf_b.cpu(),
+                                    [{k: v.cpu() for k, v in w.layers[0].items()}]))
+    for b in range(B):
+        valid = mask[b].numpy().astype(bool)
+        ref = om.layer_prefill(0, f64(x_in[b * T:(b + 1) * T]), mask[b].numpy())
+        assert_stream_close(f64(xt[b * T:(b + 1) * T])[valid], ref[valid], tol=tol,
+                            what=f"prefill layer row {b}")
+    gm.check_device()
+    gm.close()
+    del w
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_prefill_attention_ragged_tiles():
+    """Left-padded prompts of 300 slots (5 query tiles, a ragged last tile) and
+    a prompt with holes in the middle, at head width 64: every query and key
+    tile edge, pads as keys, pad queries."""
+    shape = synth.PRESETS["block"]
+    B, T = 3, 300
+    mask = torch.ones(B, T, dtype=torch.uint8)
+    mask[0, :37] = 0
+    mask[1, :129] = 0
+    mask[2, 100:140] = 0
+    _prefill_layer_vs_oracle(shape, 51, mask)
+
+
+@pytest.mark.slow
+def test_prefill_layer_7b1_at_2048_tokens():
+    """One 7b1-width layer (32 heads x 128) over a 2048-token prompt: the prefill
+    GEMM at M = 2048 and the tensor-core attention over 32 x 32 tiles."""
+    shape = synth.PRESETS["7b1"]
+    mask = torch.ones(1, 2048, dtype=torch.uint8)
+    _prefill_layer_vs_oracle(shape, 52, mask)
