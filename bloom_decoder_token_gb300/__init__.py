@@ -45,7 +45,8 @@ class BloomError(RuntimeError):
 class Config(C.Structure):
     _fields_ = [("n_layer", I32), ("hidden", I32), ("n_head", I32), ("ffn", I32),
                 ("vocab", I32), ("ln_eps", C.c_float), ("weight_dtype", I32),
-                ("max_batch", I32), ("max_tokens", I32), ("max_seq", I32), ("flags", I32)]
+                ("max_batch", I32), ("max_tokens", I32), ("max_seq", I32), ("flags", I32),
+                ("wait_us", I32)]
 
 
 class Linear(C.Structure):
@@ -170,14 +171,14 @@ class Model:
     """A BLOOM stack on the current CUDA device, weights borrowed from torch tensors."""
 
     def __init__(self, weights: synth.Weights, max_batch: int, max_tokens: int, max_seq: int,
-                 flags: int = 0, n_layer: Optional[int] = None):
+                 flags: int = 0, n_layer: Optional[int] = None, wait_us: int = 0):
         sh = weights.shape
         self.shape = sh
         self.weights = weights
         self.n_layer = len(weights.layers) if n_layer is None else n_layer
         self.device = weights.word_emb.device
         self.cfg = Config(self.n_layer, sh.hidden, sh.n_head, sh.ffn, sh.vocab, sh.ln_eps,
-                          1 if sh.int8 else 0, max_batch, max_tokens, max_seq, flags)
+                          1 if sh.int8 else 0, max_batch, max_tokens, max_seq, flags, wait_us)
         arr = (LayerWeights * self.n_layer)()
         for i in range(self.n_layer):
             L = weights.layers[i]

@@ -3,6 +3,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -52,6 +53,13 @@ void bloom::bloom_set_error(const char *fmt, ...) {
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Host-side fault injection for tests: BLOOM_INJECT_FAILURE names the
+// allocations to fail ("workspace").
+static bool inject_failure(const char *what) {
+    const char *v = getenv("BLOOM_INJECT_FAILURE");
+    return v && strstr(v, what) != nullptr;
+}
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ----------------------------------------------------------------- KV layout
@@ -175,6 +183,7 @@ static bloom_status validate_config(const bloom_config *c) {
         return fail(BLOOM_E_UNSUPPORTED, "max_batch %d (1..%d)", c->max_batch, kMaxBatch);
     if (c->max_tokens < c->max_batch) return fail(BLOOM_E_INVALID, "max_tokens < max_batch");
     if (c->max_seq < 1) return fail(BLOOM_E_INVALID, "max_seq < 1");
+    if (c->wait_us < 0) return fail(BLOOM_E_INVALID, "wait_us < 0");
     return BLOOM_OK;
 }
 
@@ -244,7 +253,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
                  o_gen = take((size_t)cfg->max_seq * MB * 4), o_ptok = take(MT * 4),
                  o_pmask = take(MT);
     m->ws_bytes = off;
-    e = cudaMalloc(&m->ws, m->ws_bytes);
+    e = inject_failure("workspace") ? cudaErrorMemoryAllocation : cudaMalloc(&m->ws, m->ws_bytes);
     if (e != cudaSuccess) {
         delete m;
         cudaGetLastError();
@@ -476,6 +485,7 @@ static void prof_mark(cudaStream_t s, int op, int kernel) {
 static GemvTcArgs tc_args(const bloom_model *m, const LinearArgs &a) {
     GemvTcArgs g;
     g.a = a;
+    g.a.wait_ns = (unsigned long long)m->cfg.wait_us * 1000ull;
     g.splits = gemv_tc_splits(a.N, a.K, a.M, a.epi, m->num_sms, a.int8);
     return g;
 }
@@ -515,7 +525,9 @@ static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wm
     cudaError_t e;
     int kernel;
     if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x) {
-        e = launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, a, s);
+        LinearArgs b = a;
+        b.wait_ns = (unsigned long long)m->cfg.wait_us * 1000ull;
+        e = launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, b, s);
         kernel = BLOOM_KERNEL_GEMM_TC;
     } else if (use_tc_linear(m, a)) {
         const int nt = gemv_tc_nt(a.M);

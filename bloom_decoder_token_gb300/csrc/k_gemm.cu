@@ -191,7 +191,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = (int)(it % kTcStages);
                     const uint32_t par = (uint32_t)((it / kTcStages) & 1);
-                    if (!tc_mbar_wait(&empty[s], par ^ 1u)) {
+                    if (!tc_mbar_wait(&empty[s], par ^ 1u, a.wait_ns)) {
                         *abort_flag = 1;
                         if (a.err) atomicOr(a.err, kErrTimeout);
                         break;
@@ -209,7 +209,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             // no copy of ours may still be landing when the CTA exits
             for (int i = 0; i < kTcStages && i < it; ++i) {
                 const long long j = it - 1 - i;
-                if (!tc_mbar_wait(&full[j % kTcStages], (uint32_t)((j / kTcStages) & 1)))
+                if (!tc_mbar_wait(&full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kTcWaitNs))
                     if (a.err) atomicOr(a.err, kErrTimeout);
             }
         }
@@ -223,7 +223,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             bool ok = true;
             for (int t = blockIdx.x; t < tiles && ok && !*abort_flag; t += gridDim.x, ++lt) {
                 const int b = lt & 1;
-                if (!tc_mbar_wait(&acc_empty[b], (uint32_t)(((lt >> 1) & 1) ^ 1))) {
+                if (!tc_mbar_wait(&acc_empty[b], (uint32_t)(((lt >> 1) & 1) ^ 1), a.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -231,7 +231,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const uint32_t acc = tmem + (uint32_t)(b * kTcBN);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = (int)(it % kTcStages);
-                    if (!tc_mbar_wait(&full[s], (uint32_t)((it / kTcStages) & 1))) {
+                    if (!tc_mbar_wait(&full[s], (uint32_t)((it / kTcStages) & 1), a.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -253,7 +253,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             }
             // every MMA of ours has finished before TMEM is freed, on every path
             tc_commit(&drained);
-            if (!tc_mbar_wait(&drained, 0) && a.err) atomicOr(a.err, kErrTimeout);
+            if (!tc_mbar_wait(&drained, 0, kTcWaitNs) && a.err) atomicOr(a.err, kErrTimeout);
         }
     } else {
         // ---- epilogue: warps 2..5 -> TMEM lane quarters (warp % 4)
@@ -267,7 +267,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc_tile_coords(t, tiles_m, tiles_n, m0, n0);
             const int m = m0 + row;
             // longer limit than the MMA issuer's, so that its commits arrive first
-            const bool ok = tc_mbar_wait(&acc_full[b], (uint32_t)((lt >> 1) & 1), 3 * kTcWaitCycles);
+            const bool ok = tc_mbar_wait(&acc_full[b], (uint32_t)((lt >> 1) & 1),
+                                         3 * (a.wait_ns ? a.wait_ns : kTcWaitNs));
             if (!ok) {
                 if (a.err) atomicOr(a.err, kErrTimeout);
                 *abort_flag = 1;

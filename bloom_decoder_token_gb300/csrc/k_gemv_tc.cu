@@ -231,7 +231,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             int issued = pre;
             for (int i = pre; i < my_kb; ++i) {
                 const int s = i % C::Stages;
-                if (!tc_mbar_wait(&empty[s], (uint32_t)(((i / C::Stages) & 1) ^ 1))) {
+                if (!tc_mbar_wait(&empty[s], (uint32_t)(((i / C::Stages) & 1) ^ 1), a.wait_ns)) {
                     s_abort = 1;
                     if (a.err) atomicOr(a.err, kErrTimeout);
                     break;
@@ -249,7 +249,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             // the CTA exits
             for (int j = 0; j < C::Stages && j < issued; ++j) {
                 const int i = issued - 1 - j;
-                if (!tc_mbar_wait(&full[i % C::Stages], (uint32_t)((i / C::Stages) & 1)) && a.err)
+                if (!tc_mbar_wait(&full[i % C::Stages], (uint32_t)((i / C::Stages) & 1), kTcWaitNs) &&
+                    a.err)
                     atomicOr(a.err, kErrTimeout);
             }
         }
@@ -261,14 +262,14 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             bool ok = true;
             for (int i = 0; i < my_kb; ++i) {
                 const int s = i % C::Stages;
-                if (!tc_mbar_wait(&full[s], (uint32_t)((i / C::Stages) & 1))) {
+                if (!tc_mbar_wait(&full[s], (uint32_t)((i / C::Stages) & 1), a.wait_ns)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sw = tc_smem(smem + (size_t)s * C::Stage);
                 if constexpr (W8) {
                     // the widened weights of this stage, in TMEM A buffer i % 2
-                    if (!tc_mbar_wait(&a_full[i & 1], (uint32_t)((i >> 1) & 1))) {
+                    if (!tc_mbar_wait(&a_full[i & 1], (uint32_t)((i >> 1) & 1), a.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -296,6 +297,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 if (a.err) atomicOr(a.err, kErrTimeout);
             }
             tc_commit(&acc_full);   // accumulator complete (or abandoned)
+            // every MMA of ours has finished before TMEM is read or freed, on every path
+            if (!tc_mbar_wait(&acc_full, 0, kTcWaitNs) && a.err) atomicOr(a.err, kErrTimeout);
         }
     }
     __syncwarp();
@@ -325,8 +328,9 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             for (int i = 0; i < my_kb; ++i) {
                 const int s = i % C::Stages;
                 const bool wok = __all_sync(
-                    0xffffffffu, tc_mbar_wait(&full[s], (uint32_t)((i / C::Stages) & 1)) &&
-                                     (i < 2 || tc_mbar_wait(&a_empty[i & 1], (uint32_t)(((i >> 1) - 1) & 1))));
+                    0xffffffffu, tc_mbar_wait(&full[s], (uint32_t)((i / C::Stages) & 1), a.wait_ns) &&
+                                     (i < 2 || tc_mbar_wait(&a_empty[i & 1], (uint32_t)(((i >> 1) - 1) & 1),
+                                                            a.wait_ns)));
                 if (!wok) {   // warp-uniform
                     s_abort = 1;
                     if (a.err) atomicOr(a.err, kErrTimeout);
@@ -380,7 +384,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
             }
         }
         // longer limit than the MMA issuer's, so that its final commit arrives first
-        const bool ok = tc_mbar_wait(&acc_full, 0, 3 * kTcWaitCycles);
+        const bool ok = tc_mbar_wait(&acc_full, 0, 3 * (a.wait_ns ? a.wait_ns : kTcWaitNs));
         if (!ok && a.err) atomicOr(a.err, kErrTimeout);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         // warp-uniform, so that the argmax shuffles below see every lane

@@ -83,6 +83,7 @@ struct LinearArgs {
     int *len_inc = nullptr;           // if set: last CTA does ++*len_inc and ++next_pos[m]
     int *next_pos = nullptr;
     int *err = nullptr;
+    unsigned long long wait_ns = 0;   // bound of the tensor-core kernels' waits (0: ~2 s)
     // fused input LayerNorm (decode, see linear_can_fuse_ln): x = LN(ln_x) with ln_g, ln_b
     const float *ln_x = nullptr;      // float [M][K] residual rows
     const uint16_t *ln_g = nullptr, *ln_b = nullptr;

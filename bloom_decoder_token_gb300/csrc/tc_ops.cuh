@@ -10,7 +10,17 @@
 
 namespace bloom {
 
-constexpr long long kTcWaitCycles = 4000000000ll;
+// Bound of every mbarrier wait unless the launch sets its own (LinearArgs::
+// wait_ns): about two seconds.  Waits for work that always finishes on its own
+// (the kernel's own copies and MMAs in flight, before it frees their memory)
+// keep this bound whatever the launch sets.
+constexpr unsigned long long kTcWaitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long tc_now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t tc_smem(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -28,13 +38,16 @@ __device__ __forceinline__ bool tc_mbar_test(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Wait for the phase `parity` of `bar` to complete, for at most limit_ns
+// nanoseconds (0: kTcWaitNs); false when the bound expired.
 __device__ __forceinline__ bool tc_mbar_wait(uint64_t *bar, uint32_t parity,
-                                             long long limit = kTcWaitCycles) {
+                                             unsigned long long limit_ns = 0) {
     if (tc_mbar_test(bar, parity)) return true;
-    const long long t0 = clock64();
+    const unsigned long long limit = limit_ns ? limit_ns : kTcWaitNs;
+    const unsigned long long t0 = tc_now_ns();
     for (uint32_t i = 1;; ++i) {
         if (tc_mbar_test(bar, parity)) return true;
-        if ((i & 15u) == 0 && clock64() - t0 > limit) return false;
+        if ((i & 15u) == 0 && tc_now_ns() - t0 > limit) return false;
     }
 }
 __device__ __forceinline__ void tc_tma_2d(void *dst, const CUtensorMap *map, int c0, int c1,

@@ -82,6 +82,12 @@ typedef struct {
     int32_t max_tokens;    /* largest B*T of any prefill (sizes the activation workspace) */
     int32_t max_seq;       /* largest cache length (prompt + generated) of any call */
     int32_t flags;         /* BLOOM_FLAG_* */
+    int32_t wait_us;       /* bound of every wait of the tensor-core kernels in microseconds,
+                              0 = about two seconds.  A wait that expires makes its launch give
+                              up (stores skipped, memory it holds freed once its own copies and
+                              MMAs have landed) and sets flag 8 for bloom_check_device; the model
+                              stays usable.  Waits for the kernel's own copies and MMAs in
+                              flight keep the default bound. */
 } bloom_config;
 
 /* One linear layer: bf16 weight, or int8 codes + bf16 row scales. */
@@ -130,7 +136,9 @@ size_t bloom_kv_bytes(const bloom_config *cfg, int32_t batch, int32_t max_seq);
 /* Validate the config and weights, compute the ALiBi slopes once (largest
  * power of two m <= n heads: 2^(-8i/m), then every other term of the 2m
  * sequence), allocate the activation workspace, and pick launch shapes.
- * The current CUDA device is the model's device.  *out is NULL on failure. */
+ * The current CUDA device is the model's device.  *out is NULL on failure.
+ * For testing the error path, the environment variable BLOOM_INJECT_FAILURE
+ * containing "workspace" makes the workspace allocation fail (BLOOM_E_OOM). */
 bloom_status bloom_create(const bloom_config *cfg, const bloom_weights *w, bloom_model **out);
 
 /* Bind `buf` (device, >= bloom_kv_bytes bytes, 256-byte aligned) as an empty
@@ -332,8 +340,9 @@ bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, int32_t M, i
  * loops may forbid allocation between requests).
  *  - M <= 256 rows; larger M returns BLOOM_E_CAPACITY and launches nothing.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress) with that device current and keeps it for the
+ *    process; make that first call before any stream capture, and make no call
+ *    after a cudaDeviceReset of that device (the kept address would be stale).
  *  - Each call clears the part of the array it uses (cudaMemsetAsync on
  *    `stream`) before its kernel; calls whose work overlaps on the GPU (other
  *    streams, other threads) share the array and race, so serialise them. */

@@ -42,7 +42,7 @@ def test_no_oracle_symbols_in_product_library(lib):
 
 def _cfg(**kw):
     base = dict(n_layer=2, hidden=1024, n_head=16, ffn=4096, vocab=512, ln_eps=1e-5,
-                weight_dtype=0, max_batch=4, max_tokens=64, max_seq=40, flags=0)
+                weight_dtype=0, max_batch=4, max_tokens=64, max_seq=40, flags=0, wait_us=0)
     base.update(kw)
     return bg.Config(*[base[f] for f, _ in bg.Config._fields_])
 
@@ -68,6 +68,7 @@ def test_kv_bytes_layout(lib):
     (dict(weight_dtype=7), 1),
     (dict(max_tokens=1), 1),
     (dict(ffn=1000), 2),
+    (dict(wait_us=-1), 1),
 ])
 def test_create_rejects_bad_config(lib, kw, status):
     c = _cfg(**kw)
