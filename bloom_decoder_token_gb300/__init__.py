@@ -63,9 +63,12 @@ class WeightsC(C.Structure):
                 ("layers", C.POINTER(LayerWeights))]
 
 
+MAX_BATCH = 256
+
+
 class KVC(C.Structure):
     _fields_ = [("buf", P), ("bytes", C.c_size_t), ("batch", I32), ("max_seq", I32),
-                ("len", I32)]
+                ("len", I32), ("row_len", I32 * MAX_BATCH), ("row_active", C.c_uint8 * MAX_BATCH)]
 
 
 _SIGS = {
@@ -74,6 +77,8 @@ _SIGS = {
     "bloom_kv_init": (I32, [P, C.POINTER(KVC), P, C.c_size_t, I32, I32, P]),
     "bloom_prefill": (I32, [P, C.POINTER(KVC), P, P, I32, I32, P, P, P]),
     "bloom_decode_step": (I32, [P, C.POINTER(KVC), P, P, P, P]),
+    "bloom_kv_admit": (I32, [P, C.POINTER(KVC), P, I32, P, P, I32, P, P, P]),
+    "bloom_kv_retire": (I32, [P, C.POINTER(KVC), P, I32, P]),
     "bloom_generate": (I32, [P, C.POINTER(KVC), P, P, I32, I32, I32, P, P]),
     "bloom_check_device": (I32, [P, P]),
     "bloom_decode_profile": (I32, [P, C.POINTER(KVC), P, P, P, P, I32, P, P]),
@@ -149,12 +154,20 @@ class KV:
     def batch(self) -> int:
         return self.c.batch
 
+    def row_len(self, b: int) -> int:
+        return self.c.row_len[b]
+
+    def row_active(self, b: int) -> bool:
+        return bool(self.c.row_active[b])
+
     def tensors(self, model: "Model"):
-        """Views of the cache regions (len, next_pos, pos, K, V) for inspection."""
+        """Views of the cache regions (len, active, next_pos, pos, K, V) for inspection."""
         sh = model.shape
         B, S = self.c.batch, self.c.max_seq
         al = lambda x: (x + 255) // 256 * 256
-        off_np = 256
+        off_len = 256
+        off_act = al(off_len + 4 * B)
+        off_np = al(off_act + 4 * B)
         off_pos = al(off_np + 4 * B)
         layer = B * sh.n_head * S * sh.head_dim * 2
         off_k = al(off_pos + 4 * B * S)
@@ -163,8 +176,8 @@ class KV:
         i32 = lambda a, n: v[a:a + 4 * n].view(torch.int32)
         bf = lambda a: v[a:a + layer * model.n_layer].view(torch.bfloat16).view(
             model.n_layer, B, sh.n_head, S, sh.head_dim)
-        return {"len": i32(0, 1), "next_pos": i32(off_np, B), "pos": i32(off_pos, B * S).view(B, S),
-                "k": bf(off_k), "v": bf(off_v)}
+        return {"len": i32(off_len, B), "active": i32(off_act, B), "next_pos": i32(off_np, B),
+                "pos": i32(off_pos, B * S).view(B, S), "k": bf(off_k), "v": bf(off_v)}
 
 
 class Model:
@@ -229,6 +242,21 @@ class Model:
         check(lib().bloom_decode_step(self.h, C.byref(kv.c), _p(next_tokens), _p(out_tokens),
                                       _p(logits), _stream(stream)))
         return out_tokens
+
+    def kv_admit(self, kv: KV, rows, tokens, mask, out_tokens=None, logits=None, stream=None):
+        """Prefill new prompts (device tokens / mask [n][T]) into cache rows `rows`."""
+        n, T = tokens.shape
+        r = (C.c_int32 * n)(*[int(v) for v in rows])
+        if out_tokens is None:
+            out_tokens = torch.empty(n, dtype=torch.int32, device=self.device)
+        check(lib().bloom_kv_admit(self.h, C.byref(kv.c), r, n, _p(tokens), _p(mask), T,
+                                   _p(out_tokens), _p(logits), _stream(stream)))
+        return out_tokens
+
+    def kv_retire(self, kv: KV, rows, stream=None):
+        """Rows `rows` leave the batch (decode steps skip them)."""
+        r = (C.c_int32 * len(rows))(*[int(v) for v in rows])
+        check(lib().bloom_kv_retire(self.h, C.byref(kv.c), r, len(rows), _stream(stream)))
 
     def generate(self, kv: KV, tokens_host, mask_host, n_new: int, out_host=None, stream=None):
         """Greedy generation from host buffers; returns host int32 [n_new, B]."""

@@ -64,13 +64,19 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // ----------------------------------------------------------------- KV layout
 struct KvLayout {
-    size_t next_pos, pos, k, v, total, layer;   // layer = bytes of one layer's K (or V)
+    size_t len, active, next_pos, pos, k, v, total, layer;   // layer = bytes of one layer's K (or V)
 };
 
+// [256-byte header][len int32[B]][active int32[B]][next_pos int32[B]]
+// [pos int32[B][S]][K bf16[L][B][n][S][d]][V ...], every region 256-byte aligned.
 static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq) {
     KvLayout L;
     const size_t d = (size_t)(c.hidden / c.n_head);
     size_t off = 256;
+    L.len = off;
+    off = align256(off + 4 * (size_t)batch);
+    L.active = off;
+    off = align256(off + 4 * (size_t)batch);
     L.next_pos = off;
     off = align256(off + 4 * (size_t)batch);
     L.pos = off;
@@ -127,6 +133,7 @@ struct bloom_model {
     int32_t *gen = nullptr;       // [max_seq][max_batch]
     int32_t *ptok = nullptr;      // [max_tokens] prompt ids (bloom_generate)
     uint8_t *pmask = nullptr;     // [max_tokens]
+    int *rowmap = nullptr;        // [max_batch] cache rows of the prompts of bloom_kv_admit
     cudaStream_t cap = nullptr;
     std::vector<GraphEntry> graphs;
     // tensor-core prefill GEMM: weight maps [layer][TC_*], activation maps TC_X_*
@@ -251,7 +258,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
                  o_ap = take(MB * n * kMaxSplits * (d + 2) * 4), o_at = take(MB * n * 4),
                  o_err = take(4), o_last = take(MB * 4), o_tok = take(MB * 4),
                  o_gen = take((size_t)cfg->max_seq * MB * 4), o_ptok = take(MT * 4),
-                 o_pmask = take(MT);
+                 o_pmask = take(MT), o_rowmap = take(MB * 4);
     m->ws_bytes = off;
     e = inject_failure("workspace") ? cudaErrorMemoryAllocation : cudaMalloc(&m->ws, m->ws_bytes);
     if (e != cudaSuccess) {
@@ -277,6 +284,7 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     m->gen = (int32_t *)(base + o_gen);
     m->ptok = (int32_t *)(base + o_ptok);
     m->pmask = (uint8_t *)(base + o_pmask);
+    m->rowmap = (int *)(base + o_rowmap);
     // ALiBi slopes, once: largest power of two p <= n heads gets 2^(-8i/p),
     // i = 1..p; the remaining heads take 2^(-8i/(2p)) for odd i = 1, 3, ...
     std::vector<float> sl(n);
@@ -400,12 +408,49 @@ extern "C" bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, s
     kv->batch = batch;
     kv->max_seq = max_seq;
     kv->len = 0;
+    for (int b = 0; b < BLOOM_MAX_BATCH; ++b) {
+        kv->row_len[b] = 0;
+        kv->row_active[b] = 0;
+    }
     return BLOOM_OK;
+}
+
+// Host mirror of the cache's per-row state: kv->len = the longest active row.
+static void kv_mirror_len(bloom_kv *kv) {
+    int mx = 0;
+    for (int b = 0; b < kv->batch; ++b)
+        if (kv->row_active[b] && kv->row_len[b] > mx) mx = kv->row_len[b];
+    kv->len = mx;
+}
+static void kv_mirror_prompt(bloom_kv *kv, const int32_t *rows, int n, int T) {
+    for (int i = 0; i < n; ++i) {
+        const int r = rows ? rows[i] : i;
+        kv->row_len[r] = T;
+        kv->row_active[r] = 1;
+    }
+    kv_mirror_len(kv);
+}
+// A decode step needs an active row, and room for one more slot in every active row.
+static bloom_status kv_check_step(const bloom_kv *kv) {
+    int active = 0;
+    for (int b = 0; b < kv->batch; ++b) {
+        if (!kv->row_active[b]) continue;
+        ++active;
+        if (kv->row_len[b] >= kv->max_seq)
+            return fail(BLOOM_E_CAPACITY, "cache row %d full (%d slots)", b, kv->max_seq);
+    }
+    if (!active) return fail(BLOOM_E_INVALID, "decode with no active sequence (prefill or admit first)");
+    return BLOOM_OK;
+}
+static void kv_mirror_step(bloom_kv *kv) {
+    for (int b = 0; b < kv->batch; ++b)
+        if (kv->row_active[b]) ++kv->row_len[b];
+    kv_mirror_len(kv);
 }
 
 // pointers into a kv buffer
 struct KvPtrs {
-    int *len, *next_pos, *pos;
+    int *len, *active, *next_pos, *pos;
     uint16_t *k, *v;
     size_t layer_elems;
 };
@@ -413,7 +458,8 @@ static KvPtrs kv_ptrs(const bloom_model *m, const bloom_kv *kv) {
     const KvLayout L = kv_layout(m->cfg, kv->batch, kv->max_seq);
     char *b = (char *)kv->buf;
     KvPtrs p;
-    p.len = (int *)b;
+    p.len = (int *)(b + L.len);
+    p.active = (int *)(b + L.active);
     p.next_pos = (int *)(b + L.next_pos);
     p.pos = (int *)(b + L.pos);
     p.k = (uint16_t *)(b + L.k);
@@ -573,7 +619,8 @@ static cudaError_t fused_ln(bloom_model *m, LinearArgs &a, const float *x, const
 // One decoder layer over M tokens.  Decode: M = B sequences, slot *len.
 // Prefill: M = B*T tokens, slots [0, T).
 static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int max_seq, int l,
-                                 int M, int T, int splits, float *x, cudaStream_t s) {
+                                 int M, int T, int splits, float *x, cudaStream_t s,
+                                 const int *row_map = nullptr) {
     const bloom_config &c = m->cfg;
     const bloom_layer_weights &L = m->layers[l];
     const int h = c.hidden, F = c.ffn, n = c.n_head, d = m->d;
@@ -585,7 +632,9 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     q.k_cache = kp.k + kp.layer_elems * l;
     q.v_cache = kp.v + kp.layer_elems * l;
     q.len_ptr = kp.len;
+    q.active = kp.active;
     q.T = T;
+    q.row_map = row_map;
     q.n_head = n;
     q.head_dim = d;
     q.max_seq = max_seq;
@@ -600,6 +649,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.pos = kp.pos;
         at.slopes = m->slopes;
         at.len_ptr = kp.len;
+        at.active = kp.active;
         at.B = B;
         at.n = n;
         at.d = d;
@@ -617,6 +667,7 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.k = q.k_cache;
         at.v = q.v_cache;
         at.pos = kp.pos;
+        at.row_map = row_map;
         at.slopes = m->slopes;
         at.B = B;
         at.T = T;
@@ -647,7 +698,8 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
 // ln_f + tied head + argmax on rows of `x` (row r at x[(r*stride + last[r]) * h]).
 static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int stride,
                                 const int *last, int32_t *out_tokens, float *logits,
-                                int *len_inc, int *next_pos, cudaStream_t s) {
+                                int *len_inc, int *next_pos, cudaStream_t s,
+                                const int *active = nullptr) {
     const bloom_config &c = m->cfg;
     LinearArgs a;
     a.w = m->word_emb;
@@ -662,6 +714,7 @@ static cudaError_t enqueue_head(bloom_model *m, const float *x, int B, int strid
     a.out_tokens = out_tokens;
     a.len_inc = len_inc;
     a.next_pos = next_pos;
+    a.active = active;
     cudaError_t e;
     if (stride == 1 && !last) {
         if ((e = fused_ln(m, a, x, m->lnf_g, m->lnf_b, s))) return e;
@@ -685,13 +738,13 @@ static cudaError_t enqueue_decode(bloom_model *m, const bloom_kv *kv, const int3
     const int splits = attn_splits(m, B, kv->max_seq);
     cudaError_t e = launch_embed(next, B, (const uint16_t *)m->word_emb, c.vocab,
                                  (const uint16_t *)m->emb_ln_g, (const uint16_t *)m->emb_ln_b,
-                                 c.hidden, c.ln_eps, m->x, kp.len, kp.next_pos, kp.pos,
+                                 c.hidden, c.ln_eps, m->x, kp.len, kp.active, kp.next_pos, kp.pos,
                                  kv->max_seq, m->err, s);
     if (e) return e;
     prof_mark(s, BLOOM_OP_EMBED, BLOOM_KERNEL_EMBED);
     for (int l = 0; l < c.n_layer; ++l)
         if ((e = enqueue_layer(m, kp, B, kv->max_seq, l, B, 0, splits, m->x, s))) return e;
-    return enqueue_head(m, m->x, B, 1, nullptr, out, logits, kp.len, kp.next_pos, s);
+    return enqueue_head(m, m->x, B, 1, nullptr, out, logits, kp.len, kp.next_pos, s, kp.active);
 }
 
 extern "C" int32_t bloom_decode_launches(const bloom_model *m, int32_t batch) {
@@ -717,9 +770,28 @@ extern "C" bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const 
     if (B != kv->batch) return fail(BLOOM_E_CAPACITY, "B=%d but kv batch is %d", B, kv->batch);
     if (T < 1 || T > kv->max_seq) return fail(BLOOM_E_CAPACITY, "T=%d outside 1..%d", T, kv->max_seq);
     const KvPtrs kp = kv_ptrs(m, kv);
-    CK(launch_prompt_setup(mask, B, T, kp.pos, kv->max_seq, kp.next_pos, m->last, kp.len, m->err,
-                           (cudaStream_t)stream));
-    kv->len = T;
+    CK(launch_prompt_setup(mask, B, T, nullptr, kp.pos, kv->max_seq, kp.next_pos, kp.len, kp.active,
+                           m->last, m->err, (cudaStream_t)stream));
+    kv_mirror_prompt(kv, nullptr, B, T);
+    return BLOOM_OK;
+}
+
+// Prefill of n prompts (tokens / mask [n][T]) into cache rows rows_dev[i]
+// (null: rows 0..n-1); the greedy token of each to out_tokens [n].
+static bloom_status prefill_rows(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
+                                 const uint8_t *mask, int32_t n, int32_t T, const int *rows_dev,
+                                 int32_t *out_tokens, float *out_logits, cudaStream_t s) {
+    const bloom_config &c = m->cfg;
+    const KvPtrs kp = kv_ptrs(m, kv);
+    const int M = n * T;
+    CK(launch_prompt_setup(mask, n, T, rows_dev, kp.pos, kv->max_seq, kp.next_pos, kp.len,
+                           kp.active, m->last, m->err, s));
+    CK(launch_embed(tokens, M, (const uint16_t *)m->word_emb, c.vocab, (const uint16_t *)m->emb_ln_g,
+                    (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, m->x, nullptr, nullptr,
+                    nullptr, nullptr, 0, m->err, s));
+    for (int l = 0; l < c.n_layer; ++l)
+        CK(enqueue_layer(m, kp, n, kv->max_seq, l, M, T, 1, m->x, s, rows_dev));
+    CK(enqueue_head(m, m->x, n, T, m->last, out_tokens, out_logits, nullptr, nullptr, s));
     return BLOOM_OK;
 }
 
@@ -734,17 +806,55 @@ extern "C" bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_
     if (T < 1 || T > kv->max_seq) return fail(BLOOM_E_CAPACITY, "T=%d outside 1..%d", T, kv->max_seq);
     if ((long long)B * T > m->cfg.max_tokens)
         return fail(BLOOM_E_CAPACITY, "B*T=%lld above max_tokens %d", (long long)B * T, m->cfg.max_tokens);
-    const bloom_config &c = m->cfg;
+    if ((st = prefill_rows(m, kv, tokens, mask, B, T, nullptr, out_tokens, out_logits,
+                           (cudaStream_t)stream)))
+        return st;
+    kv_mirror_prompt(kv, nullptr, B, T);
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_kv_admit(bloom_model *m, bloom_kv *kv, const int32_t *rows,
+                                       int32_t n, const int32_t *tokens, const uint8_t *mask,
+                                       int32_t T, int32_t *out_tokens, float *out_logits,
+                                       void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!rows || !tokens || !mask || !out_tokens) return fail(BLOOM_E_INVALID, "null argument");
+    if (n < 1 || n > kv->batch) return fail(BLOOM_E_INVALID, "n=%d outside 1..%d", n, kv->batch);
+    if (T < 1 || T > kv->max_seq) return fail(BLOOM_E_CAPACITY, "T=%d outside 1..%d", T, kv->max_seq);
+    if ((long long)n * T > m->cfg.max_tokens)
+        return fail(BLOOM_E_CAPACITY, "n*T=%lld above max_tokens %d", (long long)n * T, m->cfg.max_tokens);
+    RowList rl;
+    rl.n = n;
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] < 0 || rows[i] >= kv->batch) return fail(BLOOM_E_INVALID, "row %d", rows[i]);
+        for (int j = 0; j < i; ++j)
+            if (rows[j] == rows[i]) return fail(BLOOM_E_INVALID, "row %d given twice", rows[i]);
+        rl.rows[i] = rows[i];
+    }
     cudaStream_t s = (cudaStream_t)stream;
-    const KvPtrs kp = kv_ptrs(m, kv);
-    const int M = B * T;
-    CK(launch_prompt_setup(mask, B, T, kp.pos, kv->max_seq, kp.next_pos, m->last, kp.len, m->err, s));
-    CK(launch_embed(tokens, M, (const uint16_t *)m->word_emb, c.vocab, (const uint16_t *)m->emb_ln_g,
-                    (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, m->x, nullptr, nullptr,
-                    nullptr, 0, m->err, s));
-    for (int l = 0; l < c.n_layer; ++l) CK(enqueue_layer(m, kp, B, kv->max_seq, l, M, T, 1, m->x, s));
-    CK(enqueue_head(m, m->x, B, T, m->last, out_tokens, out_logits, nullptr, nullptr, s));
-    kv->len = T;
+    CK(launch_set_rows(rl, m->rowmap, s));
+    if ((st = prefill_rows(m, kv, tokens, mask, n, T, m->rowmap, out_tokens, out_logits, s))) return st;
+    kv_mirror_prompt(kv, rows, n, T);
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_kv_retire(bloom_model *m, bloom_kv *kv, const int32_t *rows,
+                                        int32_t n, void *stream) {
+    if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
+    bloom_status st = check_kv(m, kv);
+    if (st) return st;
+    if (!rows || n < 0 || n > kv->batch) return fail(BLOOM_E_INVALID, "rows / n=%d", n);
+    RowList rl;
+    rl.n = n;
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] < 0 || rows[i] >= kv->batch) return fail(BLOOM_E_INVALID, "row %d", rows[i]);
+        rl.rows[i] = rows[i];
+    }
+    CK(launch_set_active(rl, 0, kv_ptrs(m, kv).active, (cudaStream_t)stream));
+    for (int i = 0; i < n; ++i) kv->row_active[rows[i]] = 0;
+    kv_mirror_len(kv);
     return BLOOM_OK;
 }
 
@@ -754,8 +864,7 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!next_tokens || !out_tokens) return fail(BLOOM_E_INVALID, "null next_tokens/out_tokens");
-    if (kv->len < 1) return fail(BLOOM_E_INVALID, "decode before prefill");
-    if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full (%d slots)", kv->max_seq);
+    if ((st = kv_check_step(kv))) return st;
     cudaStream_t s = (cudaStream_t)stream;
     if (m->cfg.flags & BLOOM_FLAG_NO_GRAPH) {
         CK(enqueue_decode(m, kv, next_tokens, out_tokens, out_logits, s));
@@ -790,7 +899,7 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
         }
         CK(cudaGraphLaunch(exec, s));
     }
-    kv->len += 1;
+    kv_mirror_step(kv);
     return BLOOM_OK;
 }
 
@@ -802,8 +911,7 @@ extern "C" bloom_status bloom_decode_profile(bloom_model *m, bloom_kv *kv,
     if (st) return st;
     if (!next_tokens || !out_tokens || !codes || !ms || !n || cap < 1)
         return fail(BLOOM_E_INVALID, "null or empty argument");
-    if (kv->len < 1) return fail(BLOOM_E_INVALID, "decode before prefill");
-    if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full (%d slots)", kv->max_seq);
+    if ((st = kv_check_step(kv))) return st;
     *n = 0;
     cudaStream_t s = (cudaStream_t)stream;
     g_pdl = false;   // each launch starts after the previous one has finished
@@ -833,7 +941,7 @@ extern "C" bloom_status bloom_decode_profile(bloom_model *m, bloom_kv *kv,
     g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     CK(e);
     *n = (int32_t)std::min<size_t>(prof.ev.size(), (size_t)cap);
-    kv->len += 1;
+    kv_mirror_step(kv);
     return BLOOM_OK;
 }
 
@@ -884,10 +992,10 @@ extern "C" bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t
     if (st) return st;
     if (!x) return fail(BLOOM_E_INVALID, "null x");
     if (layer < 0 || layer >= m->cfg.n_layer) return fail(BLOOM_E_INVALID, "layer %d", layer);
-    if (kv->len >= kv->max_seq) return fail(BLOOM_E_CAPACITY, "cache full");
+    if ((st = kv_check_step(kv))) return st;
     cudaStream_t s = (cudaStream_t)stream;
     const KvPtrs kp = kv_ptrs(m, kv);
-    CK(launch_slot_pos(kv->batch, kp.len, kp.next_pos, kp.pos, kv->max_seq, m->err, s));
+    CK(launch_slot_pos(kv->batch, kp.len, kp.active, kp.next_pos, kp.pos, kv->max_seq, m->err, s));
     CK(enqueue_layer(m, kp, kv->batch, kv->max_seq, layer, kv->batch, 0,
                      attn_splits(m, kv->batch, kv->max_seq), (float *)x, s));
     return BLOOM_OK;
@@ -955,7 +1063,7 @@ extern "C" bloom_status bloom_embed(bloom_model *m, const int32_t *tokens, int32
     const bloom_config &c = m->cfg;
     CK(launch_embed(tokens, n, (const uint16_t *)m->word_emb, c.vocab, (const uint16_t *)m->emb_ln_g,
                     (const uint16_t *)m->emb_ln_b, c.hidden, c.ln_eps, (float *)x, nullptr,
-                    nullptr, nullptr, 0, m->err, (cudaStream_t)stream));
+                    nullptr, nullptr, nullptr, 0, m->err, (cudaStream_t)stream));
     return BLOOM_OK;
 }
 

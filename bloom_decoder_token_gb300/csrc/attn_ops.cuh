@@ -54,7 +54,9 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
     constexpr int NG = NT / 8;             // groups; a round covers 2 * NG keys
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = tid >> 3, sub = tid & 7;
-    const int nk = min((a.len_ptr ? *a.len_ptr : a.len_host) + 1, a.max_seq);
+    // keys [0, len] with the step's new one; an idle row appended none
+    const int nk = a.len_ptr ? min(a.len_ptr[b] + ((!a.active || a.active[b]) ? 1 : 0), a.max_seq)
+                             : min(a.len_host + 1, a.max_seq);
     const int chunk = (nk + a.splits - 1) / a.splits;
     const int k0 = split * chunk;
     const int k1 = min(nk, k0 + chunk);

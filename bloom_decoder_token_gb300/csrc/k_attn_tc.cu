@@ -90,13 +90,14 @@ __global__ void __launch_bounds__(kFaThreads) attn_prefill_tc_kernel(const AttnP
     const int g = lane >> 2, q4 = lane & 3;
     // the longest query tiles (most key tiles) first
     const int qt = gridDim.x - 1 - blockIdx.x;
-    const int j = blockIdx.y, b = blockIdx.z;
+    const int j = blockIdx.y, b = blockIdx.z;   // head, prompt
     const int q0 = qt * kFaQ;
     const int T = a.T;
-    const size_t bh = (size_t)b * a.n + j;
+    const int row = a.row_map ? a.row_map[b] : b;   // the prompt's cache row
+    const size_t bh = (size_t)row * a.n + j;
     const uint16_t *kb = a.k + bh * a.max_seq * D;
     const uint16_t *vb = a.v + bh * a.max_seq * D;
-    const int *posb = a.pos + (size_t)b * a.max_seq;
+    const int *posb = a.pos + (size_t)row * a.max_seq;
     const float slope = a.slopes[j];
     const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(fsm);
     int *spos = reinterpret_cast<int *>(fsm + L::P0);

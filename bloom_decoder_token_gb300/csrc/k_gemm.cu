@@ -84,7 +84,8 @@ __device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[3
             if (cidx == 0) {
                 o = a.q_out + (size_t)m * a.n_head * dh + (size_t)hj * dh + e0;
             } else {
-                const int seq = m / a.T, slot = m - seq * a.T;
+                const int i = m / a.T, slot = m - i * a.T;
+                const int seq = a.row_map ? a.row_map[i] : i;   // the prompt's cache row
                 if (slot >= a.max_seq) {
                     if (a.err) atomicOr(a.err, kErrSlot);
                     return;

@@ -89,13 +89,17 @@ __device__ __forceinline__ void st_dsmem4(uint32_t addr, float4 v) {
                  : "memory");
 }
 
+// The cache slot a decode token's K and V go to (staged per CTA in shared
+// memory), or kGvNoSlot for an idle row.
+constexpr int kGvNoSlot = -0x40000000;
+
 // Epilogue of J consecutive tokens m0.. of one row n (v: accumulators, the
 // bias not yet added).  The residual epilogues take the residual values in
 // `res` when the caller loaded them ahead (during the main loop), else every
 // load is issued before any store, so the J tokens cost one memory round trip.
 template <int EPI, int J>
 __device__ __forceinline__ void gv_apply(const LinearArgs &a, int m0, int mmax, int n, const float *v,
-                                         float bias, int slot, unsigned long long *best,
+                                         float bias, const int *slots, unsigned long long *best,
                                          const float *res = nullptr) {
     if constexpr (EPI == EPI_RESID32 || EPI == EPI_RESID) {
         float r[J];
@@ -134,11 +138,14 @@ __device__ __forceinline__ void gv_apply(const LinearArgs &a, int m0, int mmax, 
                 const int e = n % dh;
                 if (cidx == 0) {
                     a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e] = f2bf(x);
-                } else if (slot >= 0 && slot < a.max_seq) {
-                    uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
-                    cache[(((size_t)m * a.n_head + hj) * a.max_seq + slot) * dh + e] = f2bf(x);
-                } else if (a.err) {
-                    atomicOr(a.err, kErrSlot);
+                } else if (slots[m] != kGvNoSlot) {   // an idle row appends nothing
+                    const int slot = slots[m];
+                    if (slot >= 0 && slot < a.max_seq) {
+                        uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
+                        cache[(((size_t)m * a.n_head + hj) * a.max_seq + slot) * dh + e] = f2bf(x);
+                    } else if (a.err) {
+                        atomicOr(a.err, kErrSlot);
+                    }
                 }
             } else if constexpr (EPI == EPI_ARGMAX) {
                 if (a.logits) a.logits[o] = x;
@@ -164,6 +171,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort, s_last;
     __shared__ unsigned long long s_best[EPI == EPI_ARGMAX ? kMaxBatch : 1];
+    __shared__ int s_slot[EPI == EPI_QKV ? NT : 1];
 
     const LinearArgs &a = g.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -313,7 +321,6 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
     const int S = g.splits;
     const int groups = (mmax + 3) / 4;
     float bias = 0.f;
-    int slot = 0;
     bool live = false;
     // residuals of the token groups this CTA finishes (split, split + S, ...),
     // loaded while the main loop runs
@@ -366,7 +373,12 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
         }
         griddep_wait();   // the residual and the cache belong to earlier kernels too
         bias = (a.bias && nok) ? bf2f(a.bias[n]) : 0.f;
-        slot = (EPI == EPI_QKV && a.len_ptr) ? *a.len_ptr : 0;
+        if constexpr (EPI == EPI_QKV) {
+            const int ep = tid - 64;
+            if (ep < NT)
+                s_slot[ep] = (ep < a.M && (!a.active || a.active[ep])) ? a.len_ptr[ep] : kGvNoSlot;
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+        }
         if constexpr (kRes) {
             if (S > 1) {
 #pragma unroll
@@ -403,7 +415,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 unsigned long long best[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) best[j] = 0;   // rows past N take no part
-                if (nok) gv_apply<EPI, 16>(a, c, mmax, n, v, bias, slot, best);
+                if (nok) gv_apply<EPI, 16>(a, c, mmax, n, v, bias, s_slot, best);
                 if constexpr (EPI == EPI_ARGMAX) {
                     // max over the warp's 32 rows (every lane shuffles), then the CTA's
 #pragma unroll
@@ -471,7 +483,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                     float t[4];
                     gsum(lg, t);
                     for (int j = 0; j < 4; ++j) t[j] *= scale;
-                    gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, slot, nullptr,
+                    gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, s_slot, nullptr,
                                      kRes ? res + 4 * lg : nullptr);
                 }
             }
@@ -481,7 +493,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
                 float t[4];
                 gsum(lg, t);
                 for (int j = 0; j < 4; ++j) t[j] *= scale;
-                gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, slot, nullptr);
+                gv_apply<EPI, 4>(a, gi * 4, mmax, n, t, bias, s_slot, nullptr);
             }
         }
     }

@@ -272,8 +272,15 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
                         a.q_out[(size_t)m * a.n_head * dh + (size_t)hj * dh + e2] = f2bf(v);
                     } else {
                         int seq, slot;
-                        if (a.T > 0) { seq = m / a.T; slot = m - seq * a.T; }
-                        else { seq = m; slot = *a.len_ptr; }
+                        if (a.T > 0) {
+                            const int i = m / a.T;
+                            seq = a.row_map ? a.row_map[i] : i;
+                            slot = m - i * a.T;
+                        } else {
+                            seq = m;
+                            slot = a.len_ptr[m];
+                            if (a.active && !a.active[m]) continue;   // idle row: no append
+                        }
                         if (slot >= 0 && slot < a.max_seq) {
                             uint16_t *cache = (cidx == 1) ? a.k_cache : a.v_cache;
                             cache[(((size_t)seq * a.n_head + hj) * a.max_seq + slot) * dh + e2] =
@@ -306,13 +313,14 @@ __global__ void __launch_bounds__(kLinThreads) linear_kernel(const LinearArgs a)
             __threadfence();
             for (int i = threadIdx.x; i < a.M; i += blockDim.x) {
                 const unsigned long long p = atomicExch(&a.best[i], 0ull);
-                a.out_tokens[i] = (int)unpack_index(p);
-                if (a.len_inc) a.next_pos[i] += 1;
+                const bool act = !a.active || a.active[i];
+                a.out_tokens[i] = act ? (int)unpack_index(p) : -1;
+                if (a.len_inc && act) {
+                    a.len_inc[i] += 1;
+                    a.next_pos[i] += 1;
+                }
             }
-            if (threadIdx.x == 0) {
-                *a.ticket = 0;
-                if (a.len_inc) *a.len_inc += 1;
-            }
+            if (threadIdx.x == 0) *a.ticket = 0;
         }
     }
 }

@@ -72,15 +72,22 @@ struct LinearArgs {
     uint16_t *q_out = nullptr;        // bf16 [M][n_head * d]
     uint16_t *k_cache = nullptr;      // bf16 [Bkv][n_head][max_seq][d] (this layer)
     uint16_t *v_cache = nullptr;
-    const int *len_ptr = nullptr;     // decode: slot = *len_ptr
-    int T = 0;                        // prefill: token m is slot m % T of sequence m / T
+    // decode: token m is sequence m, appended at slot len_ptr[m] if active[m]
+    const int *len_ptr = nullptr;
+    const int *active = nullptr;
+    // prefill: token m is slot m % T of prompt m / T, which goes to cache row
+    // row_map[m / T] (row_map null: row m / T)
+    int T = 0;
+    const int *row_map = nullptr;
     int n_head = 0, head_dim = 0, max_seq = 0;
     // EPI_ARGMAX
     float *logits = nullptr;          // float [M][N] or null
     unsigned long long *best = nullptr;  // [M], zero at rest
     int *ticket = nullptr;            // zero at rest
     int *out_tokens = nullptr;        // [M]
-    int *len_inc = nullptr;           // if set: last CTA does ++*len_inc and ++next_pos[m]
+    // decode step: rows with active[m] == 0 get token -1; if len_inc is set, the
+    // last CTA advances len_inc[m] and next_pos[m] of every active row
+    int *len_inc = nullptr;
     int *next_pos = nullptr;
     int *err = nullptr;
     unsigned long long wait_ns = 0;   // bound of the tensor-core kernels' waits (0: ~2 s)
@@ -146,21 +153,34 @@ cudaError_t launch_layernorm_f32(const float *x, const uint16_t *g, const uint16
                                  int h, float eps, uint16_t *y, int src_stride, const int *last,
                                  cudaStream_t s);
 
-// Embedding gather + LN for n tokens into the float32 residual stream x.  With step state (len != null) it also
-// records the position of slot *len for each of the n sequences.
+// Embedding gather + LN for n tokens into the float32 residual stream x.  With
+// step state (len != null) it also records, for each active sequence r, the
+// position of its next slot: pos[r][len[r]] = next_pos[r].
 cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
                          const uint16_t *g, const uint16_t *b, int h, float eps, float *x,
-                         const int *len, const int *next_pos, int *pos, int max_seq, int *err,
-                         cudaStream_t s);
+                         const int *len, const int *active, const int *next_pos, int *pos,
+                         int max_seq, int *err, cudaStream_t s);
 
-// pos[b][slot=*len] = next_pos[b] for B sequences (layer-level decode entry).
-cudaError_t launch_slot_pos(int B, const int *len, const int *next_pos, int *pos, int max_seq,
-                            int *err, cudaStream_t s);
+// pos[b][len[b]] = next_pos[b] for the active ones of B sequences (layer-level
+// decode entry).
+cudaError_t launch_slot_pos(int B, const int *len, const int *active, const int *next_pos,
+                            int *pos, int max_seq, int *err, cudaStream_t s);
 
-// Prompt positions: pos[b][t] from the mask cumsum, next_pos[b], last[b] (last
-// token slot), *len = T.
-cudaError_t launch_prompt_setup(const uint8_t *mask, int B, int T, int *pos, int max_seq,
-                                int *next_pos, int *last, int *len, int *err, cudaStream_t s);
+// Prompt setup of n prompts going to cache rows row_map[i] (null: row i): pos of
+// their T slots from the mask cumsum, next_pos, len = T, active = 1 for those
+// rows, and last[i] (the prompt's last token slot).
+cudaError_t launch_prompt_setup(const uint8_t *mask, int n, int T, const int *row_map, int *pos,
+                                int max_seq, int *next_pos, int *len, int *active, int *last,
+                                int *err, cudaStream_t s);
+
+// active[rows[i]] = value for n rows given by value (n <= kMaxBatch).
+struct RowList {
+    int rows[256];
+    int n = 0;
+};
+cudaError_t launch_set_active(const RowList &r, int value, int *active, cudaStream_t s);
+// dst[i] = rows[i] for the n rows.
+cudaError_t launch_set_rows(const RowList &r, int *dst, cudaStream_t s);
 
 struct AttnDecodeArgs {
     const uint16_t *q = nullptr;     // [B][n][d]
@@ -168,7 +188,10 @@ struct AttnDecodeArgs {
     const uint16_t *v = nullptr;
     const int *pos = nullptr;        // [B][max_seq]
     const float *slopes = nullptr;   // [n]
-    const int *len_ptr = nullptr;    // keys [0, *len_ptr]; if null, keys [0, len_host]
+    // keys [0, len_ptr[b]] of an active sequence, [0, len_ptr[b]) of an idle one
+    // (active null: all active); len_ptr null: keys [0, len_host] of every sequence
+    const int *len_ptr = nullptr;
+    const int *active = nullptr;
     int len_host = 0;
     int B = 0, n = 0, d = 0, max_seq = 0;
     int splits = 1;
@@ -180,10 +203,11 @@ struct AttnDecodeArgs {
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s);
 
 struct AttnPrefillArgs {
-    const uint16_t *q = nullptr;     // [B*T][n][d]
-    const uint16_t *k = nullptr;     // [B][n][max_seq][d]
+    const uint16_t *q = nullptr;     // [B*T][n][d], prompt i's tokens at rows i*T ..
+    const uint16_t *k = nullptr;     // [rows][n][max_seq][d] (the cache)
     const uint16_t *v = nullptr;
-    const int *pos = nullptr;        // [B][max_seq]
+    const int *pos = nullptr;        // [rows][max_seq]
+    const int *row_map = nullptr;    // prompt i's cache row (null: row i)
     const float *slopes = nullptr;
     int B = 0, T = 0, n = 0, d = 0, max_seq = 0;
     float scale = 0.f;

@@ -244,13 +244,14 @@ __device__ __forceinline__ void argmax_publish(const LinearArgs &a, unsigned lon
         __threadfence();
         for (int i = tid; i < a.M; i += blockDim.x) {
             const unsigned long long p = atomicExch(&a.best[i], 0ull);
-            a.out_tokens[i] = (int)unpack_index(p);
-            if (a.len_inc) a.next_pos[i] += 1;
+            const bool act = !a.active || a.active[i];
+            a.out_tokens[i] = act ? (int)unpack_index(p) : -1;
+            if (a.len_inc && act) {   // the step appended a slot to this row
+                a.len_inc[i] += 1;
+                a.next_pos[i] += 1;
+            }
         }
-        if (tid == 0) {
-            *a.ticket = 0;
-            if (a.len_inc) *a.len_inc += 1;
-        }
+        if (tid == 0) *a.ticket = 0;
     }
 }
 

@@ -115,19 +115,26 @@ typedef struct {
 
 typedef struct bloom_model bloom_model;   /* opaque */
 
-/* KV cache: one caller-owned device allocation of bloom_kv_bytes() bytes.
- * Layout (all offsets 256-byte aligned): a 256-byte header (int32 len = slots
- * filled, shared by all sequences), int32 next_pos[batch] (ALiBi position of
- * each sequence's next token), int32 pos[batch][max_seq] (position of each
- * slot, -1 for a pad slot), then K and V, each bf16
- * [n_layer][batch][n_head][max_seq][d].  The library writes `len` here as a
- * host mirror of the device counter. */
+/* KV cache: one caller-owned device allocation of bloom_kv_bytes() bytes, one
+ * row per sequence.  Layout (all regions 256-byte aligned): a 256-byte header,
+ * int32 len[batch] (slots filled in each row), int32 active[batch] (1 = the row
+ * takes part in decode steps), int32 next_pos[batch] (ALiBi position of each
+ * row's next token), int32 pos[batch][max_seq] (position of each slot, -1 for a
+ * pad slot), then K and V, each bf16 [n_layer][batch][n_head][max_seq][d].
+ * The device copy is authoritative; the struct keeps a host mirror of the
+ * per-row state, which the library updates on every call (the caller only
+ * reads it).  Rows leave and join between decode steps (bloom_kv_retire,
+ * bloom_kv_admit): "Hugging Face BLOOM Inference Optimization", Webserver
+ * Architecture and Request Handling (dynamic batch extraction). */
+#define BLOOM_MAX_BATCH 256
 typedef struct {
     void   *buf;
     size_t  bytes;
     int32_t batch;
     int32_t max_seq;
-    int32_t len;
+    int32_t len;                              /* longest active row */
+    int32_t row_len[BLOOM_MAX_BATCH];         /* slots filled, per row */
+    uint8_t row_active[BLOOM_MAX_BATCH];      /* 1: the row decodes */
 } bloom_kv;
 
 /* Bytes a cache for `batch` sequences of `max_seq` slots needs (0 on bad args). */
@@ -142,7 +149,7 @@ size_t bloom_kv_bytes(const bloom_config *cfg, int32_t batch, int32_t max_seq);
 bloom_status bloom_create(const bloom_config *cfg, const bloom_weights *w, bloom_model **out);
 
 /* Bind `buf` (device, >= bloom_kv_bytes bytes, 256-byte aligned) as an empty
- * cache and fill *kv.  Clears the header and marks every slot a pad. */
+ * cache and fill *kv: every row empty and idle, every slot a pad. */
 bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
                            int32_t batch, int32_t max_seq, void *stream);
 
@@ -151,19 +158,38 @@ bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes
  * set slot positions (count of tokens before the slot), and emit the greedy
  * token of each row's last token slot to out_tokens int32 [B].  out_logits
  * (float [B][V]) may be NULL.  Requires B == kv->batch, T <= kv->max_seq,
- * B*T <= max_tokens.  Sets kv->len = T. */
+ * B*T <= max_tokens.  Every row becomes active with length T. */
 bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
                            const uint8_t *mask, int32_t B, int32_t T, int32_t *out_tokens,
                            float *out_logits, void *stream);
 
-/* One decode step for all kv->batch sequences: next_tokens int32 [B] go to
- * slot kv->len; out_tokens int32 [B] receives the greedy next token and may
- * alias next_tokens; out_logits float [B][V] may be NULL.  Unless
- * BLOOM_FLAG_NO_GRAPH is set, the step is captured once per distinct
- * (kv, next_tokens, out_tokens, out_logits) into a CUDA graph and replayed.
- * Increments kv->len; BLOOM_E_CAPACITY once kv->len == kv->max_seq. */
+/* One decode step: next_tokens int32 [B] of every active row go to the row's
+ * next slot (row_len); out_tokens int32 [B] receives the greedy next token of
+ * each active row and -1 for an idle one, and may alias next_tokens;
+ * out_logits float [B][V] may be NULL (idle rows' logits are meaningless).
+ * Unless BLOOM_FLAG_NO_GRAPH is set, the step is captured once per distinct
+ * (kv, next_tokens, out_tokens, out_logits) into a CUDA graph and replayed; the
+ * graph reads the rows' state on the device, so it stays valid across admit
+ * and retire.  Each active row grows by one slot; BLOOM_E_CAPACITY if an active
+ * row is full, BLOOM_E_INVALID if no row is active. */
 bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
                                int32_t *out_tokens, float *out_logits, void *stream);
+
+/* Dynamic batch: prefill n new prompts (tokens int32 [n][T], mask uint8 [n][T],
+ * device) into the cache rows rows[i] (HOST int32 [n], distinct, < kv->batch),
+ * leaving every other row untouched; those rows become active with length T
+ * and take part in the next decode steps.  out_tokens int32 [n] (device)
+ * receives each prompt's greedy token, out_logits float [n][V] may be NULL.
+ * Requires n * T <= max_tokens. */
+bloom_status bloom_kv_admit(bloom_model *m, bloom_kv *kv, const int32_t *rows, int32_t n,
+                            const int32_t *tokens, const uint8_t *mask, int32_t T,
+                            int32_t *out_tokens, float *out_logits, void *stream);
+
+/* Dynamic batch: rows rows[i] (HOST int32 [n]) leave the batch: decode steps
+ * no longer append to them (their out_tokens are -1) until an admit reuses
+ * them. */
+bloom_status bloom_kv_retire(bloom_model *m, bloom_kv *kv, const int32_t *rows, int32_t n,
+                             void *stream);
 
 /* Whole greedy generation with HOST buffers: copies tokens/mask (host int32 /
  * uint8 [B][T]) to the device, prefills, runs n_new - 1 decode steps feeding
@@ -233,13 +259,14 @@ int32_t bloom_decode_launches(const bloom_model *m, int32_t batch);
  * sum over layers and is kept unrounded; every other activation is bf16. */
 
 /* One decoder layer of the decode step on x (float [kv->batch][h], in/out) for
- * the token at slot kv->len: it writes the layer's K,V at that slot and sets
- * the slot position, but does not advance kv->len. */
+ * the next token of every active row: it writes the layer's K,V at the row's
+ * next slot and sets the slot position, but does not advance the rows. */
 bloom_status bloom_layer_decode(bloom_model *m, bloom_kv *kv, int32_t layer, void *x,
                                 void *stream);
 
 /* Set the slot positions of a prompt (mask uint8 [B][T]) in the cache and
- * kv->len = T, as the prefill does before its first layer. */
+ * make every row active with length T, as the prefill does before its first
+ * layer. */
 bloom_status bloom_kv_set_prompt(bloom_model *m, bloom_kv *kv, const uint8_t *mask,
                                  int32_t B, int32_t T, void *stream);
 

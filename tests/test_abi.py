@@ -50,12 +50,14 @@ def _cfg(**kw):
 def test_kv_bytes_layout(lib):
     c = _cfg()
     n = lib.bloom_kv_bytes(C.byref(c), 3, 40)
-    # header + next_pos + pos + 2 * layers * B * n * S * d * 2, each 256-aligned
+    # header + len + active + next_pos + pos + K + V, each 256-aligned
     al = lambda x: (x + 255) // 256 * 256
-    kv = 2 * 3 * 16 * 40 * 64 * 2
-    expect = al(al(al(256 + 4 * 3) + 4 * 3 * 40) + kv * 2)
-    expect = al(al(al(256 + 4 * 3) + 4 * 3 * 40) + kv) + kv
-    assert n == al(expect)
+    kv = 2 * 3 * 16 * 40 * 64 * 2          # layers * B * n * S * d * 2 bytes
+    off = al(256 + 4 * 3)                  # len
+    off = al(off + 4 * 3)                  # active
+    off = al(off + 4 * 3)                  # next_pos
+    off = al(off + 4 * 3 * 40)             # pos
+    assert n == al(al(off + kv) + kv)
     assert lib.bloom_kv_bytes(C.byref(c), 0, 40) == 0
 
 
