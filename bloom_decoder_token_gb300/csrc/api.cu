@@ -149,6 +149,9 @@ struct bloom_model {
     // the tensor cores: weight maps [layer][TC_*] (box 128 rows), activation maps
     // [TC_X_*][token-column class]
     bool tcb = false;
+    // every block matrix is at most one wave of unsplit tensor-core decode CTAs
+    // (two per SM), so one- and two-sequence steps run there too (use_tc_linear)
+    bool tc_small = false;
     std::vector<TcMap> dwmaps;
     TcMap dxmaps[3][kTcNtClasses];
 
@@ -332,8 +335,11 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
                  gemm_make_map(m->dxmaps[TC_X_U][ci].b, m->u, cfg->max_batch, F, 16 << ci);
         if (!ok)
             st2 = fail(BLOOM_E_CUDA, "TMA descriptors for the decode linears could not be encoded");
-        else
+        else {
             m->tcb = true;
+            const int widest = std::max(3 * h, F);
+            m->tc_small = (widest + bw - 1) / bw <= 2 * m->num_sms;
+        }
     }
     // TMA descriptors of every bf16 weight and of the activations the prefill GEMMs read
     if (!st2 && !i8 && !(cfg->flags & BLOOM_FLAG_NO_TC_GEMM) && cfg->max_tokens >= kTcMinM) {
@@ -484,11 +490,15 @@ static LinearArgs lin_args(const bloom_linear &l, int int8, const uint16_t *x, i
 }
 
 // Whether the LayerNorm feeding `a` would be fused into the weight-streaming
-// kernel (decode, 1-2 rows).  There the fused launch beats the tensor-core
-// kernel plus a LayerNorm launch, so QKV, up and the head stay on it.
+// kernel (decode, 1-2 rows), which then beats a tensor-core kernel plus a
+// LayerNorm launch: the LM head (one pass over 2 GB, where the streaming
+// kernel reaches the copy peak), the int8 QKV and up projections, and the bf16
+// ones of stacks too wide for tc_small.  Other bf16 block linears run on the
+// tensor-core kernel at every batch size (see use_tc_linear).
 static bool prefers_ln_fusion(const bloom_model *m, const LinearArgs &a) {
     return !(m->cfg.flags & BLOOM_FLAG_NO_LN_FUSION) && linear_can_fuse_ln(a) &&
-           (a.epi == EPI_QKV || a.epi == EPI_GELU || a.epi == EPI_ARGMAX);
+           (a.epi == EPI_ARGMAX ||
+            ((a.int8 || !m->tc_small) && (a.epi == EPI_QKV || a.epi == EPI_GELU)));
 }
 
 // The LM head + argmax on the tensor cores (one pass over the embedding; no K split).
@@ -542,19 +552,23 @@ static cudaError_t run_tc_head(bloom_model *m, const LinearArgs &a, cudaStream_t
     return launch_gemv_tc(m->head_wmap.b, m->head_xmaps[ci].b, tc_args(m, a), nt, s);
 }
 
-// A decode block linear on the tensor-core decode kernel: bf16 weights, from
-// kTcBlockMinM sequences.  Measured per kernel on GB300 (7b1 shapes, launches
-// back to back, 8 / 32 tokens, tensor-core kernel vs weight-streaming kernel):
-// QKV 18.9 / 21.4 vs 21.8 / 33.0 us, dense 9.3 / 11.9 vs 9.6 / 14.3, up
-// 23.9 / 26.4 vs 30.4 / 48.6, down 24.8 / 28.2 vs 34.3 / 48.5.  At one or two
-// sequences the whole step stays on the weight-streaming kernel (QKV and up
-// with the LayerNorm fused): its CTAs take no shared memory, so each launch
-// becomes resident beside its predecessor and starts streaming early; a
-// tensor-core kernel between them (two 108 KB CTAs per SM) blocks that, and
-// the 7b1 step at one sequence took 4.17 ms instead of 3.18.
-constexpr int kTcBlockMinM = 3;
+// A decode block linear on the tensor-core decode kernel.  Measured on GB300
+// (7b1, 30 layers, whole decode step): bf16 at one / two sequences 3.11 / 3.11
+// ms with every block linear there (LayerNorm as its own launch) vs 3.18 / 3.64
+// ms on the weight-streaming kernel with the LayerNorm fused into QKV and up,
+// and 4.13 / 4.39 ms with only dense and down moved: the streaming kernel's
+// CTAs start early beside a predecessor that takes no shared memory, which a
+// tensor-core kernel (two 108 KB CTAs per SM) in between prevents, so the two
+// kernels do not mix within a layer at one or two sequences.  That holds where
+// the widest block matrix is one wave of unsplit tensor-core CTAs (tc_small);
+// the 176B-layer stack (448 tiles for up) at one sequence took 12.99 ms on the
+// tensor-core kernel vs 12.14 streaming, and stays there below
+// kTcSmallBatchMinM sequences, as int8 does (it widens the codes in registers
+// at the copy rate there; the tensor-core form converts through TMEM).
+constexpr int kTcSmallBatchMinM = 3;
 static bool use_tc_linear(const bloom_model *m, const LinearArgs &a) {
-    return m->tcb && a.T == 0 && !a.ln_x && a.M >= kTcBlockMinM && a.M <= m->cfg.max_batch &&
+    const int min_m = (a.int8 || !m->tc_small) ? kTcSmallBatchMinM : 1;
+    return m->tcb && a.T == 0 && !a.ln_x && a.M >= min_m && a.M <= m->cfg.max_batch &&
            (!a.int8 || a.M <= kGvInt8MaxNt) && !prefers_ln_fusion(m, a);
 }
 

@@ -11,12 +11,17 @@
 //
 // The block takes one contiguous key range.  Inside it, groups of 8 lanes run
 // an online softmax (running max m, sum l, accumulator) over their own keys,
-// two keys in flight per group; lane `sub` of a group owns d/8 elements of q
-// and of the accumulator, so a key costs one 3-step shuffle for the dot
-// product and no other communication.  Groups merge by shuffles, warps through
-// shared memory, and the last block of a (sequence, head) to finish merges the
-// split partials by rescaling with exp(m_split - m_max) -- no second pass and
-// no waiting.
+// kAttnKeysPerGroup keys in flight per group; lane `sub` of a group owns d/8
+// elements of q and of the accumulator, so a key costs one 3-step shuffle for
+// the dot product and no other communication.  Groups merge by shuffles, warps
+// through shared memory, and the last block of a (sequence, head) to finish
+// merges the split partials by rescaling with exp(m_split - m_max) -- no second
+// pass and no waiting.
+//
+// The launch fixes an upper bound on the split count (the graph of a decode
+// step is captured once for every length); a block derives the split count it
+// uses from the live key count, at least kAttnMinKeysPerSplit keys a split, and
+// blocks beyond it return at once.
 #pragma once
 
 #include <math.h>
@@ -37,6 +42,9 @@ __device__ __forceinline__ void softmax_merge(float &m, float &l, float *acc, in
     m = M;
 }
 
+constexpr int kAttnKeysPerGroup = 2;       // keys in flight per 8-lane group
+constexpr int kAttnMinKeysPerSplit = 32;   // a split takes at least this many keys
+
 template <int D, int NT>
 struct AttnSmem {
     float m[NT / 32], l[NT / 32];
@@ -51,13 +59,16 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
                                                   AttnSmem<D, NT> &sm) {
     constexpr int EPT = D / 8;             // elements per lane of an 8-lane group
     constexpr int NW = NT / 32;
-    constexpr int NG = NT / 8;             // groups; a round covers 2 * NG keys
+    constexpr int NG = NT / 8;             // groups; a round covers kAttnKeysPerGroup * NG keys
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = tid >> 3, sub = tid & 7;
     // keys [0, len] with the step's new one; an idle row appended none
     const int nk = a.len_ptr ? min(a.len_ptr[b] + ((!a.active || a.active[b]) ? 1 : 0), a.max_seq)
                              : min(a.len_host + 1, a.max_seq);
-    const int chunk = (nk + a.splits - 1) / a.splits;
+    int chunk = (nk + a.splits - 1) / a.splits;
+    if (chunk < kAttnMinKeysPerSplit) chunk = kAttnMinKeysPerSplit;
+    const int splits = nk > 0 ? (nk + chunk - 1) / chunk : 1;   // uniform over the blocks of (b, j)
+    if (split >= splits) return;
     const int k0 = split * chunk;
     const int k1 = min(nk, k0 + chunk);
 
@@ -79,66 +90,67 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
         }
     }
     float m_run = -INFINITY, l_run = 0.f;
-    const int rounds = (k1 - k0 + 2 * NG - 1) / (2 * NG);
+    constexpr int KPG = kAttnKeysPerGroup;
+    const int rounds = (k1 - k0 + KPG * NG - 1) / (KPG * NG);
     for (int r = 0; r < rounds; ++r) {
-        const int ka = k0 + r * 2 * NG + grp, kb = ka + NG;
-        const bool la = ka < k1, lb = kb < k1;
-        uint4 kva[EPT / 8], kvb[EPT / 8], vva[EPT / 8], vvb[EPT / 8];
-        int pa = -1, pb = -1;
-        if (la) {
-            pa = posb[ka];
+        bool live[KPG];
+        int pk[KPG];
+        uint4 kv[KPG][EPT / 8], vv[KPG][EPT / 8];
 #pragma unroll
-            for (int i = 0; i < EPT / 8; ++i) {
-                kva[i] = *reinterpret_cast<const uint4 *>(kbase + (size_t)ka * D + 8 * i);
-                vva[i] = *reinterpret_cast<const uint4 *>(vbase + (size_t)ka * D + 8 * i);
+        for (int u = 0; u < KPG; ++u) {
+            const int key = k0 + (r * KPG + u) * NG + grp;
+            live[u] = key < k1;
+            pk[u] = -1;
+            if (live[u]) {
+                pk[u] = posb[key];
+#pragma unroll
+                for (int i = 0; i < EPT / 8; ++i) {
+                    kv[u][i] = *reinterpret_cast<const uint4 *>(kbase + (size_t)key * D + 8 * i);
+                    vv[u][i] = *reinterpret_cast<const uint4 *>(vbase + (size_t)key * D + 8 * i);
+                }
             }
         }
-        if (lb) {
-            pb = posb[kb];
+        float sc[KPG];
 #pragma unroll
-            for (int i = 0; i < EPT / 8; ++i) {
-                kvb[i] = *reinterpret_cast<const uint4 *>(kbase + (size_t)kb * D + 8 * i);
-                vvb[i] = *reinterpret_cast<const uint4 *>(vbase + (size_t)kb * D + 8 * i);
+        for (int u = 0; u < KPG; ++u) {
+            float d = 0.f;
+            if (live[u]) {
+#pragma unroll
+                for (int i = 0; i < EPT / 8; ++i) {
+                    float f[8];
+                    unpack8(kv[u][i], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) d = fmaf(qf[8 * i + e], f[e], d);
+                }
             }
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            sc[u] = (live[u] && pk[u] >= 0) ? d + slope * (float)pk[u] : -INFINITY;
         }
-        float da = 0.f, db = 0.f;
+        float m_new = m_run;
 #pragma unroll
-        for (int i = 0; i < EPT / 8; ++i) {
-            float f[8];
-            if (la) {
-                unpack8(kva[i], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) da = fmaf(qf[8 * i + e], f[e], da);
-            }
-            if (lb) {
-                unpack8(kvb[i], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) db = fmaf(qf[8 * i + e], f[e], db);
-            }
-        }
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) {
-            da += __shfl_xor_sync(0xffffffffu, da, o);
-            db += __shfl_xor_sync(0xffffffffu, db, o);
-        }
-        const float sa = (la && pa >= 0) ? da + slope * (float)pa : -INFINITY;
-        const float sb = (lb && pb >= 0) ? db + slope * (float)pb : -INFINITY;
-        const float m_new = fmaxf(m_run, fmaxf(sa, sb));
+        for (int u = 0; u < KPG; ++u) m_new = fmaxf(m_new, sc[u]);
         if (m_new == -INFINITY) continue;   // uniform within the group
         const float corr = (m_run == -INFINITY) ? 0.f : expf(m_run - m_new);
-        const float wa = (sa == -INFINITY) ? 0.f : expf(sa - m_new);
-        const float wb = (sb == -INFINITY) ? 0.f : expf(sb - m_new);
-        l_run = l_run * corr + wa + wb;
+        float wt[KPG];
+        l_run *= corr;
 #pragma unroll
-        for (int i = 0; i < EPT / 8; ++i) {
-            float fa[8], fb[8];
-            if (wa != 0.f) unpack8(vva[i], fa);
-            else for (int e = 0; e < 8; ++e) fa[e] = 0.f;
-            if (wb != 0.f) unpack8(vvb[i], fb);
-            else for (int e = 0; e < 8; ++e) fb[e] = 0.f;
+        for (int u = 0; u < KPG; ++u) {
+            wt[u] = (sc[u] == -INFINITY) ? 0.f : expf(sc[u] - m_new);
+            l_run += wt[u];
+        }
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[8 * i + e] = fmaf(wb, fb[e], fmaf(wa, fa[e], acc[8 * i + e] * corr));
+        for (int e = 0; e < EPT; ++e) acc[e] *= corr;
+#pragma unroll
+        for (int u = 0; u < KPG; ++u) {
+            if (wt[u] == 0.f) continue;   // masked or absent key: adds exactly nothing
+#pragma unroll
+            for (int i = 0; i < EPT / 8; ++i) {
+                float f[8];
+                unpack8(vv[u][i], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[8 * i + e] = fmaf(wt[u], f[e], acc[8 * i + e]);
+            }
         }
         m_run = m_new;
     }
@@ -176,7 +188,7 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
             A = fmaf(sm.acc[w][tid], wgt, A);
         }
     }
-    if (a.splits == 1) {
+    if (splits == 1) {
         if (tid < D) a.o[(size_t)b * a.n * D + (size_t)j * D + tid] = f2bf(L > 0.f ? A / L : 0.f);
         return;
     }
@@ -188,17 +200,17 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
     }
     __threadfence();
     __syncthreads();
-    if (tid == 0) sm.last = (atomicAdd(a.ticket + bh, 1) == a.splits - 1);
+    if (tid == 0) sm.last = (atomicAdd(a.ticket + bh, 1) == splits - 1);
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
     if (tid < D) {
         const float *pb = a.part + bh * a.splits * (D + 2);
         float Mx = -INFINITY;
-        for (int sp = 0; sp < a.splits; ++sp) Mx = fmaxf(Mx, __ldcg(pb + sp * (D + 2)));
+        for (int sp = 0; sp < splits; ++sp) Mx = fmaxf(Mx, __ldcg(pb + sp * (D + 2)));
         float Ls = 0.f, As = 0.f;
         if (Mx != -INFINITY) {
-            for (int sp = 0; sp < a.splits; ++sp) {
+            for (int sp = 0; sp < splits; ++sp) {
                 const float ms = __ldcg(pb + sp * (D + 2));
                 if (ms == -INFINITY) continue;
                 const float wgt = expf(ms - Mx);

@@ -215,13 +215,17 @@ def test_decode_qkv_through_tcgen05():
 
 
 @pytest.mark.parametrize("B", [1, 2, 3])
-def test_decode_small_batch_through_tcgen05(B):
-    """One to three sequences: dense and down (and from three sequences QKV, up
-    and the head) on the tensor-core decode kernel, QKV / up / head on the
-    weight-streaming kernel with the LayerNorm fused at one and two."""
+@pytest.mark.parametrize("flags", [0, bg.FLAG_NO_TC_GEMM], ids=["tcgen05", "streaming"])
+def test_decode_small_batch_through_tcgen05(B, flags):
+    """One to three sequences of a stack narrow enough for the tensor-core
+    decode kernel at every batch size.  Default: every block linear there
+    (LayerNorm launches of their own), the head on the weight-streaming kernel
+    with ln_f fused at one and two sequences and on the tensor-core kernel from
+    three.  Streaming: QKV, up and the head with the LayerNorm fused at one and
+    two sequences."""
     shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000, batch=B, prompt=8, ragged=True)
     w = synth.make_weights(shape, seed=31 + B, random_affine=True)
-    generate_parity(shape, w, steps=3, tol=2e-2)
+    generate_parity(shape, w, steps=3, tol=2e-2, flags=flags)
 
 
 # The 176B-layer matrices at full size (QKV 43008 x 14336, up 57344 x 14336,
