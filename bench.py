@@ -349,6 +349,43 @@ def prefill_flops(sh: synth.Shape, B: int, T: int) -> float:
     return lin + att + head
 
 
+def op_gemm_line(shape: str, dev, bg, reps: int = 0):
+    """One prefill GEMM (bloom_op_gemm, bias, no activation) of M x N x K at
+    bf16, timed with CUDA events over launches alternating between two weight
+    copies (together larger than L2 for the shapes of interest), beside
+    torch.nn.functional.linear (cuBLAS) on the same operands."""
+    M, N, K = (int(v) for v in shape.split("x"))
+    g = torch.Generator(device=dev).manual_seed(5)
+    x = torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16)
+    ws = [(torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16) for _ in range(2)]
+    b = torch.zeros(N, device=dev, dtype=torch.bfloat16)
+    y = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+    flop = 2.0 * M * N * K
+    reps = reps or max(5, min(200, int(2e13 / flop)))
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        c = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            fn(i)
+        c.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(c) / reps
+
+    ms = timed(lambda i: bg.op_gemm(x, ws[i % 2], bias=b, y=y))
+    ms_ref = timed(lambda i: torch.nn.functional.linear(x, ws[i % 2], b))
+    peak, src = bf16_peak()
+    tf = flop / (ms / 1e3) / 1e12
+    return {"shape": shape, "ms": ms, "tflops": tf, "peak_tflops": peak, "frac": tf / peak,
+            "peak_source": src, "cublas_ms": ms_ref, "cublas_tflops": flop / (ms_ref / 1e3) / 1e12,
+            "reps": reps}
+
+
 def prefill_extra(name, B, T, dev, args, bg):
     """Whole prefill of B prompts of T tokens through bloom_prefill on a preset
     stack (its own model, freed afterwards): time (CUDA events), TFLOP/s and
@@ -603,6 +640,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-only", default=None, metavar="PRESET:BxT",
                     help="only time one whole prefill, e.g. 176b14:4x2048, and print its line")
+    ap.add_argument("--op-gemm", default=None, metavar="MxNxK",
+                    help="only time one prefill GEMM of this shape (and cuBLAS beside it)")
+    ap.add_argument("--op-reps", type=int, default=0, help="launches timed by --op-gemm (0: by size)")
     ap.add_argument("--no-extras", action="store_true",
                     help="only the workload itself (no batch series, int8 or 176B-shape keys)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
@@ -624,6 +664,11 @@ def main():
         sh = sh.with_(prompt=args.prompt)
     if args.impl == "reference":
         run_reference(args, sh)
+    elif args.op_gemm:
+        import bloom_decoder_token_gb300 as bg
+        torch.cuda.set_device(0)
+        print(json.dumps({"op_gemm": op_gemm_line(args.op_gemm, torch.device("cuda", 0), bg,
+                                                  args.op_reps)}), flush=True)
     elif args.prefill_only:
         import bloom_decoder_token_gb300 as bg
         name, bt = args.prefill_only.split(":")
