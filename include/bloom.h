@@ -65,8 +65,10 @@ enum {
                                     the decode linear kernel that consumes it */
     BLOOM_FLAG_NO_TC_GEMM = 8    /* every linear on the weight-streaming kernel instead of the
                                     tensor-core (tcgen05) kernels: the prefill GEMM (>= 128
-                                    tokens), the decode LM head (>= 8 sequences) and the wide
-                                    or long bf16 decode block linears (>= 8 sequences) */
+                                    tokens), the decode LM head (>= 3 sequences) and the decode
+                                    block linears (bf16: every batch size where each block matrix
+                                    is at most one wave of 128-row tiles, else >= 3 sequences;
+                                    int8: 3..128 sequences) */
 };
 
 typedef struct {
