@@ -167,6 +167,40 @@ def num_threads() -> int:
     return int(lib().orc_num_threads())
 
 
+def sample_top_p(logits, temperature: float, top_p: float, u: float) -> int:
+    """Per-member sampling of one row, float64, from its definition.
+
+    "Hugging Face BLOOM Inference Optimization", Webserver Architecture and
+    Request Handling: the custom generation loop applies each batch member's
+    own sampling parameters (temperature, top-p).  Top-p (nucleus) sampling:
+    p = softmax(logits / temperature); sort the tokens by probability, highest
+    first (equal probabilities: lower index first); the nucleus is the shortest
+    prefix of that order whose probabilities sum to at least top_p; the
+    distribution renormalised over the nucleus is sampled by inverting its
+    cumulative sum, taken in vocabulary order, at the caller's uniform number
+    u in [0, 1) (the random number is an input, so both sides draw the same).
+    temperature <= 0 is greedy: the argmax, lowest index on ties.  top_p >= 1
+    keeps every token.
+    """
+    z = as_f64(logits).ravel()
+    V = z.shape[0]
+    if not temperature > 0.0:
+        return int(np.flatnonzero(z == z.max())[0])
+    p = np.exp((z - z.max()) / temperature)
+    p = p / p.sum()
+    order = np.lexsort((np.arange(V), -p))           # probability desc, index asc
+    cum = np.cumsum(p[order])
+    n = V if top_p >= 1.0 else min(V, int(np.searchsorted(cum, top_p, side="left")) + 1)
+    keep = np.zeros(V, dtype=bool)
+    keep[order[:n]] = True
+    q = np.where(keep, p, 0.0)
+    c = np.cumsum(q / q.sum())                        # vocabulary order
+    i = int(np.searchsorted(c, u, side="right"))      # first index with c > u
+    if i >= V:                                        # u at the top of the rounding
+        i = int(np.flatnonzero(keep)[-1])
+    return i
+
+
 # ---------------------------------------------------------------- whole model
 class Model:
     """Oracle view of a ``synth.Weights`` stack (bits copied to the host)."""

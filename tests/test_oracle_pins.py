@@ -238,3 +238,73 @@ def test_prefill_taps_and_decode_taps_consistent():
     # a layer applied on its own reproduces the next tap
     x1 = om.layer_prefill(0, taps[0][1], mask[1].numpy())
     np.testing.assert_allclose(x1, taps[1][1], rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- top-p sampling
+LN2, LN3 = math.log(2.0), math.log(3.0)
+
+
+def test_sample_closed_form():
+    # logits 0, ln 2, ln 3 -> p = 1/6, 1/3, 1/2
+    z = [0.0, LN2, LN3]
+    # top_p 0.5: the most probable token alone reaches it
+    for u in (0.0, 0.3, 0.999):
+        assert orc.sample_top_p(z, 1.0, 0.5, u) == 2
+    # top_p 0.51: nucleus {2, 1} of mass 5/6, renormalised 0, 0.4, 0.6 in vocabulary order
+    assert orc.sample_top_p(z, 1.0, 0.51, 0.39) == 1
+    assert orc.sample_top_p(z, 1.0, 0.51, 0.41) == 2
+    # top_p 1: cumulative 1/6, 1/2, 1 in vocabulary order
+    assert orc.sample_top_p(z, 1.0, 1.0, 0.1) == 0
+    assert orc.sample_top_p(z, 1.0, 1.0, 0.3) == 1
+    assert orc.sample_top_p(z, 1.0, 1.0, 0.9) == 2
+
+
+def test_sample_temperature_scales_logits():
+    z = np.array([0.0, LN2, LN3, -1.0])
+    for u in np.linspace(0.0, 0.999, 37):
+        for tp in (0.4, 0.8, 1.0):
+            assert orc.sample_top_p(2.0 * z, 2.0, tp, u) == orc.sample_top_p(z, 1.0, tp, u)
+
+
+def test_sample_greedy_and_tiny_nucleus():
+    assert orc.sample_top_p([1.0, 3.0, 3.0, 2.0], 0.0, 0.9, 0.5) == 1   # greedy, lowest index
+    assert orc.sample_top_p([1.0, 3.0, 3.0, 2.0], -1.0, 0.9, 0.5) == 1
+    z = np.random.default_rng(3).normal(size=50)
+    top = int(np.argmax(z))
+    for u in (0.0, 0.5, 0.99):
+        assert orc.sample_top_p(z, 0.7, 1e-9, u) == top
+
+
+def test_sample_ties_enter_the_nucleus_by_index():
+    # p = e, e, e, 1 over 3e + 1: the ordering keeps ties in index order, so the
+    # two-token nucleus is {0, 1}, renormalised 1/2, 1/2
+    z = [1.0, 1.0, 1.0, 0.0]
+    assert orc.sample_top_p(z, 1.0, 0.5, 0.49) == 0
+    assert orc.sample_top_p(z, 1.0, 0.5, 0.51) == 1
+    assert orc.sample_top_p(z, 1.0, 0.5, 0.99) == 1
+
+
+@pytest.mark.parametrize("seed,top_p,temp", [(0, 0.7, 1.0), (1, 0.3, 0.5), (2, 0.95, 1.7)])
+def test_sample_distribution_by_brute_force(seed, top_p, temp):
+    """Over a fine grid of u, each token is drawn with its probability
+    renormalised over the nucleus, and the nucleus is the smallest set of
+    most-probable tokens reaching top_p -- found here by enumerating subsets."""
+    rng = np.random.default_rng(seed)
+    z = rng.normal(size=6) * 2.0
+    p = np.exp(z / temp - np.max(z / temp))
+    p /= p.sum()
+    best = None
+    for mask in range(1, 64):
+        idx = [i for i in range(6) if mask >> i & 1]
+        mass = p[idx].sum()
+        if mass >= top_p and (best is None or len(idx) < len(best[0]) or
+                              (len(idx) == len(best[0]) and mass > best[1])):
+            best = (idx, mass)
+    nucleus, mass = best
+    want = np.zeros(6)
+    want[nucleus] = p[nucleus] / mass
+    n = 20000
+    got = np.zeros(6)
+    for u in (np.arange(n) + 0.5) / n:
+        got[orc.sample_top_p(z, temp, top_p, u)] += 1
+    np.testing.assert_allclose(got / n, want, atol=2.0 / n)
