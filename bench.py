@@ -457,6 +457,73 @@ def kernel_shares(gm, sh, B, T, dev, reps=3):
     return rows, total, keys
 
 
+def sampling_extra(gm, sh, B, T, S, ids_d, mask_d, dev, stream, bg, hbm):
+    """Per-member temperature + top-p sampling on the bench workload: the
+    sampling kernel alone on B rows of V float32 logits (CUDA events; bytes =
+    one read of the logits + the per-row parameters and tokens), and decode
+    steps with sampling (logits written, then sampled) against greedy ones."""
+    V = sh.vocab
+    g = torch.Generator().manual_seed(3)
+    temps = (0.5 + torch.rand(B, generator=g)).to(dev)
+    tops = torch.full((B,), 0.9).to(dev)
+    u = torch.rand(B, generator=g).to(dev)
+    lg = torch.empty(B, V, dtype=torch.float32, device=dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    n = min(20, S - T - 1)
+
+    def steps(sampled):
+        kv = gm.new_kv(B, S)
+        gm.prefill(kv, ids_d, mask_d, out_tokens=tok)
+        for _ in range(2):   # warm-up (graph capture)
+            if sampled:
+                gm.decode_step_sampled(kv, tok, temps, tops, u, lg, out_tokens=tok)
+            else:
+                gm.decode_step(kv, tok, tok, logits=lg)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n - 2):
+            if sampled:
+                gm.decode_step_sampled(kv, tok, temps, tops, u, lg, out_tokens=tok)
+            else:
+                gm.decode_step(kv, tok, tok, logits=lg)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / (n - 2)
+
+    greedy_ms = steps(False)
+    sampled_ms = steps(True)
+    line = op_sample_line(lg, temps, tops, u, dev, stream, bg, hbm)
+    line.update({"workload": f"{sh.name}: B {B}, V {V} (the step's logits), temperature 0.5-1.5, "
+                             f"top-p 0.9",
+                 "decode_step_ms_greedy_with_logits": greedy_ms,
+                 "decode_step_ms_sampled": sampled_ms})
+    return line
+
+
+def op_sample_line(lg, temps, tops, u, dev, stream, bg, hbm, reps: int = 20):
+    """The sampling kernel alone on these logits (CUDA events); its bytes are
+    one read of the logits plus the per-row parameters and tokens."""
+    B, V = lg.shape
+    out = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        bg.op_sample(lg, temps, tops, u, out=out)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        bg.op_sample(lg, temps, tops, u, out=out)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    us = a.elapsed_time(b) / reps * 1e3
+    nbytes = B * V * 4 + B * 16
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"sample_kernel_us": us, "bytes_per_launch": nbytes, "achieved_gbs": gbs,
+            "frac_of_hbm": gbs / hbm}
+
+
 def extra_stack(name, batches, dev, args, bg, hbm):
     """Decode series of another preset (its own model, freed afterwards)."""
     sh = synth.PRESETS[name]
@@ -575,6 +642,7 @@ def run_ours(args, sh):
     extras = {}
     if series:
         extras["decode_by_batch"] = decode_series(gm, sh, series, dev, stream, hbm)
+        extras["sampling"] = sampling_extra(gm, sh, B, T, S, ids_d, mask_d, dev, stream, bg, hbm)
     gm.close()
     del gm, kv
     torch.cuda.synchronize(dev)
@@ -643,6 +711,9 @@ def main():
     ap.add_argument("--op-gemm", default=None, metavar="MxNxK",
                     help="only time one prefill GEMM of this shape (and cuBLAS beside it)")
     ap.add_argument("--op-reps", type=int, default=0, help="launches timed by --op-gemm (0: by size)")
+    ap.add_argument("--op-sample", default=None, metavar="BxV",
+                    help="only time the sampling kernel on B rows of V seeded logits "
+                         "(N(0, 2), temperature 0.5-1.5, top-p 0.9)")
     ap.add_argument("--no-extras", action="store_true",
                     help="only the workload itself (no batch series, int8 or 176B-shape keys)")
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
@@ -669,6 +740,20 @@ def main():
         torch.cuda.set_device(0)
         print(json.dumps({"op_gemm": op_gemm_line(args.op_gemm, torch.device("cuda", 0), bg,
                                                   args.op_reps)}), flush=True)
+    elif args.op_sample:
+        import bloom_decoder_token_gb300 as bg
+        torch.cuda.set_device(0)
+        dev = torch.device("cuda", 0)
+        B, V = (int(v) for v in args.op_sample.split("x"))
+        g = torch.Generator().manual_seed(3)
+        lg = (torch.randn(B, V, generator=g) * 2.0).to(dev)
+        temps = (0.5 + torch.rand(B, generator=g)).to(dev)
+        tops = torch.full((B,), 0.9).to(dev)
+        u = torch.rand(B, generator=g).to(dev)
+        hbm, _ = peaks()
+        line = op_sample_line(lg, temps, tops, u, dev, torch.cuda.current_stream(dev), bg, hbm)
+        line["shape"] = args.op_sample
+        print(json.dumps({"op_sample": line}), flush=True)
     elif args.prefill_only:
         import bloom_decoder_token_gb300 as bg
         name, bt = args.prefill_only.split(":")

@@ -77,6 +77,7 @@ _SIGS = {
     "bloom_kv_init": (I32, [P, C.POINTER(KVC), P, C.c_size_t, I32, I32, P]),
     "bloom_prefill": (I32, [P, C.POINTER(KVC), P, P, I32, I32, P, P, P]),
     "bloom_decode_step": (I32, [P, C.POINTER(KVC), P, P, P, P]),
+    "bloom_decode_step_sampled": (I32, [P, C.POINTER(KVC), P, P, P, P, P, P, P]),
     "bloom_kv_admit": (I32, [P, C.POINTER(KVC), P, I32, P, P, I32, P, P, P]),
     "bloom_kv_retire": (I32, [P, C.POINTER(KVC), P, I32, P]),
     "bloom_generate": (I32, [P, C.POINTER(KVC), P, P, I32, I32, I32, P, P]),
@@ -97,6 +98,7 @@ _SIGS = {
     "bloom_op_linear_tc": (I32, [C.POINTER(Linear), I32, P, I32, I32, I32, I32, P, P]),
     "bloom_op_attn_decode": (I32, [P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P]),
     "bloom_op_lmhead_argmax": (I32, [P, P, I32, I32, I32, P, P, P]),
+    "bloom_op_sample": (I32, [P, I32, I32, C.c_int64, P, P, P, P, P]),
     "bloom_op_lmhead_argmax_noalloc": (I32, [P, P, I32, I32, I32, P, P, P]),
 }
 EXPORTS = tuple(_SIGS)
@@ -243,6 +245,18 @@ class Model:
                                       _p(logits), _stream(stream)))
         return out_tokens
 
+    def decode_step_sampled(self, kv: KV, next_tokens, temperature, top_p, u, logits,
+                            out_tokens=None, stream=None):
+        """One decode step, then each active row's token sampled with its own
+        temperature / top-p at the caller's uniform u (device float32 [B] each;
+        logits: device float32 [B][V] scratch, written)."""
+        if out_tokens is None:
+            out_tokens = torch.empty(kv.batch, dtype=torch.int32, device=self.device)
+        check(lib().bloom_decode_step_sampled(self.h, C.byref(kv.c), _p(next_tokens),
+                                              _p(out_tokens), _p(logits), _p(temperature),
+                                              _p(top_p), _p(u), _stream(stream)))
+        return out_tokens
+
     def kv_admit(self, kv: KV, rows, tokens, mask, out_tokens=None, logits=None, stream=None):
         """Prefill new prompts (device tokens / mask [n][T]) into cache rows `rows`."""
         n, T = tokens.shape
@@ -379,6 +393,17 @@ def op_lmhead_argmax(x, emb, logits: bool = True, stream=None):
     check(lib().bloom_op_lmhead_argmax(_p(x), _p(emb), M, V, K, _p(tok), _p(lg),
                                        _stream(stream)))
     return tok, lg
+
+
+def op_sample(logits, temperature, top_p, u, out=None, stream=None):
+    """Temperature + top-p sampling of float32 logits [B][V] (rows may be
+    strided) with per-row device float32 [B] temperature, top_p, u."""
+    B, V = logits.shape
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    check(lib().bloom_op_sample(_p(logits), B, V, logits.stride(0), _p(temperature), _p(top_p),
+                                _p(u), _p(out), _stream(stream)))
+    return out
 
 
 def op_lmhead_argmax_noalloc(x, emb, logits: bool = True, stream=None):

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbloom.so")
-SOURCES = ["api.cu", "k_linear.cu", "k_norm.cu", "k_attn.cu", "k_attn_tc.cu", "noalloc.cu", "k_gemm.cu", "k_gemv_tc.cu"]
+SOURCES = ["api.cu", "k_linear.cu", "k_norm.cu", "k_attn.cu", "k_attn_tc.cu", "noalloc.cu", "k_gemm.cu", "k_gemv_tc.cu", "k_sample.cu"]
 HEADERS = ["common.cuh", "kernels.h", "tile_ops.cuh", "attn_ops.cuh", "norm_ops.cuh", "tc_ops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

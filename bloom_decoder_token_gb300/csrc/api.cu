@@ -1232,6 +1232,49 @@ extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
     return BLOOM_OK;
 }
 
+extern "C" bloom_status bloom_op_sample(const float *logits, int32_t B, int32_t V, int64_t ld,
+                                        const float *temperature, const float *top_p,
+                                        const float *u, int32_t *out_tokens, void *stream) {
+    g_pdl = true;
+    if (!logits || !temperature || !top_p || !u || !out_tokens)
+        return fail(BLOOM_E_INVALID, "null argument");
+    if (B < 1 || B > 65535 || V < 1 || ld < V)
+        return fail(BLOOM_E_INVALID, "B=%d V=%d ld=%lld", B, V, (long long)ld);
+    SampleArgs a;
+    a.logits = logits;
+    a.ld = ld;
+    a.B = B;
+    a.V = V;
+    a.temperature = temperature;
+    a.top_p = top_p;
+    a.u = u;
+    a.out = out_tokens;
+    CK(launch_sample(a, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_decode_step_sampled(bloom_model *m, bloom_kv *kv,
+                                                  const int32_t *next_tokens, int32_t *out_tokens,
+                                                  float *logits, const float *temperature,
+                                                  const float *top_p, const float *u,
+                                                  void *stream) {
+    if (!logits || !temperature || !top_p || !u) return fail(BLOOM_E_INVALID, "null argument");
+    bloom_status st = bloom_decode_step(m, kv, next_tokens, out_tokens, logits, stream);
+    if (st) return st;
+    SampleArgs a;
+    a.logits = logits;
+    a.ld = m->cfg.vocab;
+    a.B = kv->batch;
+    a.V = m->cfg.vocab;
+    a.temperature = temperature;
+    a.top_p = top_p;
+    a.u = u;
+    a.active = kv_ptrs(m, kv).active;
+    a.out = out_tokens;
+    CK(launch_sample(a, (cudaStream_t)stream));
+    return BLOOM_OK;
+}
+
 extern "C" bloom_status bloom_op_lmhead_argmax(const void *x, const void *emb, int32_t M,
                                                int32_t V, int32_t K, int32_t *out_tokens,
                                                float *out_logits, void *stream) {

@@ -202,6 +202,21 @@ struct AttnDecodeArgs {
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s);
 
+// Per-member temperature + top-p sampling of B rows of float32 logits
+// (k_sample.cu): row b's logits at logits + b * ld, its temperature, top-p and
+// uniform number u in [0, 1) at index b of the three arrays; out[b] = token.
+struct SampleArgs {
+    const float *logits = nullptr;
+    long long ld = 0;
+    int B = 0, V = 0;
+    const float *temperature = nullptr;
+    const float *top_p = nullptr;
+    const float *u = nullptr;
+    const int32_t *active = nullptr;   // optional: rows with active[b] == 0 get -1
+    int32_t *out = nullptr;
+};
+cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s);
+
 struct AttnPrefillArgs {
     const uint16_t *q = nullptr;     // [B*T][n][d], prompt i's tokens at rows i*T ..
     const uint16_t *k = nullptr;     // [rows][n][max_seq][d] (the cache)

@@ -177,6 +177,19 @@ bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
 bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
                                int32_t *out_tokens, float *out_logits, void *stream);
 
+/* Per-member sampling (temperature + top-p) after the LM head: one decode step
+ * (bloom_decode_step, logits into `logits`, float [B][V], device, required),
+ * then each active row's next token drawn from its logits by bloom_op_sample
+ * with its own temperature[b], top_p[b] and uniform number u[b] (device float
+ * [B] each; the caller draws u, so the same inputs give the same tokens) into
+ * out_tokens; idle rows get -1.  "Hugging Face BLOOM Inference
+ * Optimization", Webserver Architecture and Request Handling: the custom
+ * generation loop applies each batch member's own sampling parameters. */
+bloom_status bloom_decode_step_sampled(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
+                                       int32_t *out_tokens, float *logits,
+                                       const float *temperature, const float *top_p,
+                                       const float *u, void *stream);
+
 /* Dynamic batch: prefill n new prompts (tokens int32 [n][T], mask uint8 [n][T],
  * device) into the cache rows rows[i] (HOST int32 [n], distinct, < kv->batch),
  * leaving every other row untouched; those rows become active with length T
@@ -347,6 +360,23 @@ bloom_status bloom_op_attn_decode(const void *q, const void *k_cache, const void
                                   const int32_t *pos, const float *slopes, int32_t B,
                                   int32_t n_head, int32_t d, int32_t max_seq, int32_t len,
                                   int32_t splits, void *o, void *stream);
+
+/* Temperature + top-p sampling of B rows of float32 logits (row b at logits +
+ * b * ld, ld >= V; device).  temperature, top_p, u: device float [B]; out_tokens:
+ * device int32 [B].  Row b: p_i proportional to exp((z_i - max z) / temperature);
+ * the nucleus is the shortest prefix of the tokens by probability (highest
+ * first, equal logits in index order) whose mass reaches top_p; the token is
+ * where the nucleus's cumulative mass in vocabulary order first exceeds u times
+ * its mass.  temperature <= 0 or NaN: greedy argmax (lowest index on ties);
+ * top_p >= 1 or NaN: every token with non-zero mass; top_p <= 0: the most
+ * probable token; u < 0 or NaN counts as 0, u >= 1 takes the last nucleus
+ * token.  Masses are 2^-40 fixed point of float32 exp, summed in 64-bit
+ * integers: the result does not depend on summation order.  NaN logits take no
+ * part.  One CTA of 1024 threads per row; BLOOM_E_INVALID for null pointers,
+ * B outside 1..65535, V < 1 or ld < V. */
+bloom_status bloom_op_sample(const float *logits, int32_t B, int32_t V, int64_t ld,
+                             const float *temperature, const float *top_p, const float *u,
+                             int32_t *out_tokens, void *stream);
 
 /* Tied LM head with fused argmax: logits[m][v] = x[m] . E[v]; out_tokens[m] =
  * lowest index of the row maximum of the float32 logits; out_logits may be

@@ -179,12 +179,12 @@ def sample_top_p(logits, temperature: float, top_p: float, u: float) -> int:
     distribution renormalised over the nucleus is sampled by inverting its
     cumulative sum, taken in vocabulary order, at the caller's uniform number
     u in [0, 1) (the random number is an input, so both sides draw the same).
-    temperature <= 0 is greedy: the argmax, lowest index on ties.  top_p >= 1
-    keeps every token.
+    temperature <= 0 is greedy: the argmax, lowest index on ties (so is a row
+    with no finite maximum).  top_p >= 1 keeps every token.
     """
     z = as_f64(logits).ravel()
     V = z.shape[0]
-    if not temperature > 0.0:
+    if not temperature > 0.0 or not np.isfinite(z.max()):
         return int(np.flatnonzero(z == z.max())[0])
     p = np.exp((z - z.max()) / temperature)
     p = p / p.sum()
