@@ -1,4 +1,5 @@
-// Per-member temperature + top-p sampling after the LM head, one row per CTA.
+// Per-member temperature + top-p sampling after the LM head; one cluster of
+// kSmpCluster CTAs per row, each CTA a contiguous slice of the vocabulary.
 //
 // "Hugging Face BLOOM Inference Optimization", Webserver Architecture and
 // Request Handling: the generation loop applies each batch member's own
@@ -16,23 +17,25 @@
 // (float32; 0 once the exponent passes 27, where it is below 2^-38), summed
 // in 64-bit integers, so every sum, cut and comparison is exact and
 // independent of the summation order: the same logits give the same token on
-// every run.  The nucleus cut
-// (the logit t* of its last token) is found by narrowing:
-//  1. a 2048-bin histogram of mass and count over d_i = (max z - z_i) / t,
+// every run.  The nucleus cut (the logit t* of its last token) is found by
+// narrowing:
+//  1. a 2048-bin histogram of mass over d_i = (max z - z_i) / t,
 //     spread over the row's own range of d, and the bin where the cumulative
 //     mass (bins in order of d) reaches ceil(p * total);
 //  2. if that bin holds more than kSmpCand tokens: a second 2048-bin histogram
 //     over the order-preserving keys of its logits, and the sub-bin where the
 //     mass is reached (a bin of one logit value is the cut at once);
-//  3. the region's tokens sorted by (logit desc, index asc) in shared memory
-//     and scanned to the cut -- or, for a region of more than kSmpCand tokens
-//     (only heavy repetition of a few logit values), a bisection over its key
-//     range;
+//  3. the region's tokens sorted by (logit desc, index asc) in the first CTA's
+//     shared memory and scanned to the cut -- or, for a region of more than
+//     kSmpCand tokens (only heavy repetition of a few logit values), a
+//     bisection over its key range;
 //  4. the tokens with logit t* enter in index order, as many as the mass still
 //     missing needs.
 // A last pass over contiguous index chunks scans the nucleus masses in
-// vocabulary order (block scans in thread order) and the thread holding the
-// sampled position walks its chunk to the token.
+// vocabulary order (block scans in thread order, then over the cluster in
+// rank order) and the thread holding the sampled position walks its chunk to
+// the token.  Every histogram, total and scan is combined across the cluster
+// through distributed shared memory, in rank order.
 #include <math.h>
 #include <stdint.h>
 
@@ -41,24 +44,62 @@
 
 namespace bloom {
 
-constexpr int kSmpThreads = 1024;
+constexpr int kSmpCluster = 8;                 // CTAs per row
+constexpr int kSmpThreads = 512;
 constexpr int kSmpWarps = kSmpThreads / 32;
 constexpr int kSmpBins = 2048;
-constexpr int kSmpCand = 4096;                 // bin elements sorted in shared memory
+constexpr int kSmpCand = 4096;                 // region tokens sorted in shared memory
 constexpr float kSmpScale = 1099511627776.f;   // 2^40: fixed-point unit of mass
 constexpr float kSmpDmax = 27.f;               // d beyond this: mass 0 (exp(-27) * 2^40 > 2)
+constexpr int kSmpXch = 16;                    // exchange slots (u64) per CTA
 
 struct SmpSmem {
-    unsigned long long hmass[kSmpBins];
-    unsigned int hcount[kSmpBins];
-    unsigned long long cand[kSmpCand];         // (~key << 32) | index, ascending = key desc, index asc
+    unsigned long long hmass[kSmpBins];        // this CTA's histogram
+    unsigned long long hsum[kSmpBins];         // the cluster's
+    unsigned long long cand[kSmpCand];         // (~key << 32) | index: ascending = key desc, index asc
     unsigned long long wsum[kSmpWarps];
+    unsigned long long xch[kSmpXch];           // values the peers read
     float wmax[kSmpWarps], wmin[kSmpWarps];
     int widx[kSmpWarps];
     unsigned long long bcast[4];
     int ibcast[4];
     unsigned int ncand;
 };
+
+// ---- cluster helpers
+__device__ __forceinline__ void smp_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t smp_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t smp_map(const void *p, uint32_t rank) {
+    const uint32_t local = (uint32_t)__cvta_generic_to_shared(p);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ unsigned long long smp_ld64(uint32_t a) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned int smp_ld32(uint32_t a) {
+    unsigned int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void smp_st64(uint32_t a, unsigned long long v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int smp_atom_add(uint32_t a, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+    return old;
+}
 
 // order-preserving key of a float (NaN never reaches it)
 __device__ __forceinline__ uint32_t smp_key(float f) {
@@ -91,6 +132,37 @@ __device__ __forceinline__ bool smp_live(float z, float zmax, float rt, float in
     return live;
 }
 
+// Calls f(i, z[i]) for this thread's indices of [s0, s1) (i = s0 + tid, then
+// steps of kSmpThreads, ascending), eight loads in flight at a time.
+template <typename F>
+__device__ __forceinline__ void smp_each(const float *z, int s0, int s1, F &&f) {
+    for (int i0 = s0 + (int)threadIdx.x; i0 < s1; i0 += 8 * kSmpThreads) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + k * kSmpThreads;
+            v[k] = i < s1 ? z[i] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + k * kSmpThreads;
+            if (i < s1) f(i, v[k]);
+        }
+    }
+}
+// The same over this thread's contiguous chunk [c0, c1), in index order.
+template <typename F>
+__device__ __forceinline__ void smp_chunk(const float *z, int c0, int c1, F &&f) {
+    for (int i0 = c0; i0 < c1; i0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = i0 + k < c1 ? z[i0 + k] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (i0 + k < c1) f(i0 + k, v[k]);
+    }
+}
+
 // Exclusive scan of one 64-bit value per thread in thread order; every thread
 // gets its prefix, `total` the sum.  Contains barriers.
 __device__ __forceinline__ unsigned long long smp_scan(unsigned long long v, SmpSmem &sm,
@@ -106,90 +178,128 @@ __device__ __forceinline__ unsigned long long smp_scan(unsigned long long v, Smp
     if (lane == 31) sm.wsum[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        unsigned long long w = sm.wsum[lane];
+        unsigned long long w = lane < kSmpWarps ? sm.wsum[lane] : 0ull;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        sm.wsum[lane] = w;   // inclusive
+        if (lane < kSmpWarps) sm.wsum[lane] = w;   // inclusive
     }
     __syncthreads();
     total = sm.wsum[kSmpWarps - 1];
     return (warp ? sm.wsum[warp - 1] : 0ull) + x - v;
 }
 
-// Sum of one 64-bit value per thread.  Contains barriers.
-__device__ __forceinline__ unsigned long long smp_sum(unsigned long long v, SmpSmem &sm) {
-    unsigned long long total;
-    smp_scan(v, sm, total);
-    return total;
+// Cluster-wide exclusive prefix (in rank order) and total of one value per CTA
+// (the value of thread 0), through exchange slot `slot`: every slot is written
+// once per launch.  Contains a cluster barrier.
+__device__ __forceinline__ unsigned long long smp_cluster_scan(unsigned long long v, int slot,
+                                                               SmpSmem &sm, uint32_t rank,
+                                                               unsigned long long &total) {
+    if (threadIdx.x == 0) sm.xch[slot] = v;
+    smp_cluster_sync();
+    unsigned long long pre = 0ull, tot = 0ull;
+#pragma unroll
+    for (int r = 0; r < kSmpCluster; ++r) {
+        const unsigned long long x = smp_ld64(smp_map(&sm.xch[slot], (uint32_t)r));
+        if ((uint32_t)r < rank) pre += x;
+        tot += x;
+    }
+    total = tot;
+    return pre;
 }
 
-// The bin of sm.hmass where the cumulative mass (bins in index order) reaches
-// `target` (1 .. the total), and the mass of the bins before it; two bins per
-// thread.  Contains barriers.
+// Combines one value per CTA (thread 0's) over the cluster through exchange
+// slot `slot` (written once per launch): max (op 0) or min (op 1) of u64.
+// Contains a cluster barrier.
+__device__ __forceinline__ unsigned long long smp_cluster_combine(unsigned long long v, int slot,
+                                                                  int op, SmpSmem &sm) {
+    if (threadIdx.x == 0) sm.xch[slot] = v;
+    smp_cluster_sync();
+    unsigned long long r = op == 0 ? 0ull : ~0ull;
+#pragma unroll
+    for (int k = 0; k < kSmpCluster; ++k) {
+        const unsigned long long x = smp_ld64(smp_map(&sm.xch[slot], (uint32_t)k));
+        r = op == 0 ? (x > r ? x : r) : (x < r ? x : r);
+    }
+    return r;
+}
+
+// The cluster's histogram: every rank's hmass summed in rank order into hsum.
+// The caller has synchronised the cluster after the histograms were built.
+__device__ __forceinline__ void smp_merge(SmpSmem &sm) {
+    for (int bin = threadIdx.x; bin < kSmpBins; bin += kSmpThreads) {
+        unsigned long long m = 0ull;
+#pragma unroll
+        for (int r = 0; r < kSmpCluster; ++r) m += smp_ld64(smp_map(&sm.hmass[bin], (uint32_t)r));
+        sm.hsum[bin] = m;
+    }
+    __syncthreads();
+}
+
+// In the merged histogram: the bin where the cumulative mass (bins in index
+// order) reaches `target` (1 .. the total), and the mass before it; each
+// thread takes kSmpBins / kSmpThreads consecutive bins.  Contains barriers.
 __device__ __forceinline__ void smp_select(unsigned long long target, SmpSmem &sm, int &bin,
                                            unsigned long long &before) {
-    const int tid = threadIdx.x;
-    const unsigned long long m0 = sm.hmass[2 * tid], m1 = sm.hmass[2 * tid + 1];
+    constexpr int BPT = kSmpBins / kSmpThreads;
+    const int b0 = threadIdx.x * BPT;
+    unsigned long long mine = 0ull;
+#pragma unroll
+    for (int k = 0; k < BPT; ++k) mine += sm.hsum[b0 + k];
     unsigned long long tot;
-    const unsigned long long pre = smp_scan(m0 + m1, sm, tot);
-    if (pre < target && pre + m0 + m1 >= target) {
-        const bool first = pre + m0 >= target;
-        sm.ibcast[0] = first ? 2 * tid : 2 * tid + 1;
-        sm.bcast[0] = first ? pre : pre + m0;
+    unsigned long long run = smp_scan(mine, sm, tot);
+    if (run < target && run + mine >= target) {
+#pragma unroll
+        for (int k = 0; k < BPT; ++k) {
+            const unsigned long long m = sm.hsum[b0 + k];
+            if (run < target && run + m >= target) {
+                sm.ibcast[0] = b0 + k;
+                sm.bcast[0] = run;
+            }
+            run += m;
+        }
     }
     __syncthreads();
     bin = sm.ibcast[0];
     before = sm.bcast[0];
 }
 
-// Block-wide minimum and maximum of one 32-bit key per thread.  Contains barriers.
-__device__ __forceinline__ void smp_minmax(uint32_t lo, uint32_t hi, SmpSmem &sm, uint32_t &mn,
-                                           uint32_t &mxk) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    __syncthreads();   // the scratch may still be read by a previous call
-    if (lane == 0) sm.wsum[warp] = ((unsigned long long)hi << 32) | lo;
+// Zeroes this CTA's histogram.  Contains a barrier.
+__device__ __forceinline__ void smp_clear(SmpSmem &sm) {
+    for (int i = threadIdx.x; i < kSmpBins; i += kSmpThreads) sm.hmass[i] = 0ull;
     __syncthreads();
-    mn = 0xffffffffu;
-    mxk = 0u;
-    for (int w = 0; w < kSmpWarps; ++w) {
-        mn = min(mn, (uint32_t)sm.wsum[w]);
-        mxk = max(mxk, (uint32_t)(sm.wsum[w] >> 32));
-    }
 }
 
-__global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs a) {
+__global__ void __launch_bounds__(kSmpThreads) sample_kernel(const SampleArgs a) {
     extern __shared__ __align__(16) unsigned char smp_raw[];
     SmpSmem &sm = *reinterpret_cast<SmpSmem *>(smp_raw);
     griddep_launch();
     griddep_wait();   // the logits come from the previous kernel
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x;
-    const int V = a.V;
-    const float *z = a.logits + (size_t)b * a.ld;
-    if (a.active && !a.active[b]) {   // an idle row of a dynamic batch
-        if (tid == 0) a.out[b] = -1;
+    const uint32_t rank = smp_rank();
+    const int b = blockIdx.y;
+    if (a.active && !a.active[b]) {   // an idle row of a dynamic batch (the whole cluster)
+        if (rank == 0 && tid == 0) a.out[b] = -1;
         return;
     }
+    const int V = a.V;
+    const int per = (V + kSmpCluster - 1) / kSmpCluster;
+    const int s0 = min(V, (int)rank * per), s1 = min(V, s0 + per);   // this CTA's slice
+    const float *z = a.logits + (size_t)b * a.ld;
+    if (tid == 0) sm.ncand = 0u;   // the first CTA's candidate counter (ordered by the next cluster barrier)
 
-    // ---- maximum (and its lowest index), minimum
+    // ---- maximum (lowest index on ties) and minimum over the row
     float mx = -INFINITY, mn = INFINITY;
     int mi = 0x7fffffff;
-    for (int i = tid; i < V; i += kSmpThreads) {
-        const float v = z[i];
+    smp_each(z, s0, s1, [&](int i, float v) {
         if (v > mx) {   // NaN never wins; i ascends, so a thread keeps its lowest index
             mx = v;
             mi = i;
         }
         if (v < mn) mn = v;
-    }
+    });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, mx, o);
@@ -216,36 +326,48 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs
         }
         mn = fminf(mn, sm.wmin[w]);
     }
+    {
+        // larger logit first, then the lower index: (key << 32) | ~index, maximised
+        const unsigned long long pk =
+            ((unsigned long long)smp_key(mx) << 32) | (unsigned int)(0xffffffffu - (unsigned int)mi);
+        const unsigned long long best = smp_cluster_combine(pk, 0, 0, sm);
+        const unsigned long long low = smp_cluster_combine(smp_key(mn), 1, 1, sm);
+        mx = smp_unkey((uint32_t)(best >> 32));
+        mi = (int)(0xffffffffu - (uint32_t)best);
+        mn = smp_unkey((uint32_t)low);
+    }
     const float t = a.temperature[b];
-    if (!(t > 0.f) || !(mx > -INFINITY) || mx == INFINITY) {   // greedy (or nothing to sample)
-        if (tid == 0) a.out[b] = mi == 0x7fffffff ? 0 : mi;
+    const bool greedy = !(t > 0.f) || !(mx > -INFINITY) || mx == INFINITY;
+    if (greedy) {   // greedy (or nothing to sample)
+        if (rank == 0 && tid == 0) a.out[b] = mi == 0x7fffffff ? 0 : mi;
+        smp_cluster_sync();   // no CTA leaves while a peer may still read its exchange slots
         return;
     }
     const float tp = a.top_p[b];
     float u = a.u[b];
     if (!(u >= 0.f)) u = 0.f;
-    // first-level bins spread over the row's range of d (at most kSmpDmax)
     const float rt = 1.f / t;
+    // first-level bins spread over the row's range of d (at most kSmpDmax)
     const float span = fminf(kSmpDmax, (mx - mn) * rt);
     const float inv = span > 0.f ? (float)kSmpBins / span : 0.f;
 
-    // ---- total mass and the first-level histogram
-    for (int i = tid; i < kSmpBins; i += kSmpThreads) {
-        sm.hmass[i] = 0ull;
-        sm.hcount[i] = 0u;
-    }
-    __syncthreads();
-    unsigned long long mine = 0ull;
-    for (int i = tid; i < V; i += kSmpThreads) {
+    // ---- first-level histogram of the slice, merged over the cluster
+    smp_clear(sm);
+    smp_each(z, s0, s1, [&](int i, float v) {
         int bin;
-        const unsigned long long q = smp_mass(z[i], mx, rt, inv, bin);
-        if (q) {
-            mine += q;
-            atomicAdd(&sm.hmass[bin], q);
-            atomicAdd(&sm.hcount[bin], 1u);
-        }
+        const unsigned long long q = smp_mass(v, mx, rt, inv, bin);
+        if (q) atomicAdd(&sm.hmass[bin], q);
+    });
+    __syncthreads();
+    smp_cluster_sync();
+    smp_merge(sm);
+    // total mass Q (> 0: the maximum has mass 2^40) and the target ceil(p * Q)
+    unsigned long long Q;
+    {
+        unsigned long long mine = 0ull;
+        for (int k = tid; k < kSmpBins; k += kSmpThreads) mine += sm.hsum[k];
+        smp_scan(mine, sm, Q);
     }
-    const unsigned long long Q = smp_sum(mine, sm);   // > 0: the maximum has mass 2^40
     unsigned long long target = Q;
     if (tp < 1.f) {
         const double want = ceil((double)(tp > 0.f ? tp : 0.f) * (double)Q);
@@ -255,67 +377,92 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs
     int b1;
     unsigned long long above1;
     smp_select(target, sm, b1, above1);
-    const unsigned int n1 = sm.hcount[b1];
+    // tokens in bin b1 (a pass without atomics, summed over the block and the cluster)
+    unsigned long long n1;
+    {
+        unsigned long long c = 0ull;
+        smp_each(z, s0, s1, [&](int i, float v) {
+            int bin;
+            if (smp_live(v, mx, rt, inv, bin) && bin == b1) ++c;
+        });
+        unsigned long long cta;
+        smp_scan(c, sm, cta);
+        smp_cluster_scan(cta, 4, sm, rank, n1);
+    }
 
     // ---- the region of the cut: bin b1, or one of its second-level sub-bins
     bool level2 = false;
-    uint32_t kmin = 0u, krange_m1 = 0u;   // second level: keys kmin .. kmin + krange_m1
-    int s2 = 0;                           // the sub-bin (by key, ascending)
-    unsigned long long base = above1;     // mass of the tokens above the region
-    unsigned int nreg = n1;
-    uint32_t rlo = 0u, rhi = 0xffffffffu; // key bounds of the region (second level)
+    unsigned long long base = above1;      // mass of the tokens above the region
+    unsigned long long nreg = n1;
+    uint32_t rlo = 0u, rhi = 0xffffffffu;  // key bounds of a second-level region
     uint32_t tkey = 0u;
     unsigned long long mass_gt = 0ull;
     bool cut_found = false;
-    if (n1 > (unsigned int)kSmpCand) {
+    if (n1 > (unsigned long long)kSmpCand) {
         uint32_t lo = 0xffffffffu, hi = 0u;
-        for (int i = tid; i < V; i += kSmpThreads) {
-            const float v = z[i];
+        smp_each(z, s0, s1, [&](int i, float v) {
             int bin;
             if (smp_live(v, mx, rt, inv, bin) && bin == b1) {
                 const uint32_t k = smp_key(v);
                 lo = min(lo, k);
                 hi = max(hi, k);
             }
+        });
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
         }
-        uint32_t kmax;
-        smp_minmax(lo, hi, sm, kmin, kmax);
+        if (lane == 0) sm.wsum[warp] = ((unsigned long long)hi << 32) | lo;
+        __syncthreads();
+        lo = 0xffffffffu;
+        hi = 0u;
+        for (int w = 0; w < kSmpWarps; ++w) {
+            lo = min(lo, (uint32_t)sm.wsum[w]);
+            hi = max(hi, (uint32_t)(sm.wsum[w] >> 32));
+        }
+        const uint32_t kmin = (uint32_t)smp_cluster_combine(lo, 2, 1, sm);
+        const uint32_t kmax = (uint32_t)smp_cluster_combine(hi, 3, 0, sm);
         if (kmin == kmax) {   // one logit value: the cut is there
             tkey = kmin;
             mass_gt = above1;
             cut_found = true;
         } else {
             level2 = true;
-            krange_m1 = kmax - kmin;
-            const unsigned long long range = (unsigned long long)krange_m1 + 1ull;
-            __syncthreads();
-            for (int i = tid; i < kSmpBins; i += kSmpThreads) {
-                sm.hmass[i] = 0ull;
-                sm.hcount[i] = 0u;
-            }
-            __syncthreads();
-            for (int i = tid; i < V; i += kSmpThreads) {
-                const float v = z[i];
-                int bin;
+            const unsigned long long range = (unsigned long long)(kmax - kmin) + 1ull;
+            smp_clear(sm);   // every peer finished merging the first level (cluster barriers since)
+            smp_each(z, s0, s1, [&](int i, float v) {
+                    int bin;
                 const unsigned long long q = smp_mass(v, mx, rt, inv, bin);
                 if (q && bin == b1) {
                     // sub-bins in descending key order, so that the walk runs from the top
                     const int sb = kSmpBins - 1 -
                                    (int)((unsigned long long)(smp_key(v) - kmin) * kSmpBins / range);
                     atomicAdd(&sm.hmass[sb], q);
-                    atomicAdd(&sm.hcount[sb], 1u);
                 }
-            }
+            });
             __syncthreads();
+            smp_cluster_sync();
+            smp_merge(sm);
             int b2;
             unsigned long long above2;
             smp_select(target - above1, sm, b2, above2);
-            s2 = kSmpBins - 1 - b2;
+            const int s2 = kSmpBins - 1 - b2;
             base = above1 + above2;
-            nreg = sm.hcount[b2];
-            // keys k of sub-bin s2: floor((k - kmin) * 2048 / range) == s2
+            // the keys k of sub-bin s2: floor((k - kmin) * 2048 / range) == s2
             rlo = kmin + (uint32_t)(((unsigned long long)s2 * range + kSmpBins - 1) / kSmpBins);
             rhi = kmin + (uint32_t)(((unsigned long long)(s2 + 1) * range + kSmpBins - 1) / kSmpBins) - 1u;
+            unsigned long long c = 0ull;
+            smp_each(z, s0, s1, [&](int i, float v) {
+                    int bin;
+                if (smp_live(v, mx, rt, inv, bin) && bin == b1) {
+                    const uint32_t k = smp_key(v);
+                    c += (k >= rlo && k <= rhi) ? 1ull : 0ull;
+                }
+            });
+            unsigned long long cta;
+            smp_scan(c, sm, cta);
+            smp_cluster_scan(cta, 5, sm, rank, nreg);
         }
     }
     auto in_region = [&](float v, int bin) {
@@ -326,98 +473,109 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs
     };
     if (!cut_found) {
         const unsigned long long need = target - base;   // 1 .. the region's mass
-        if (nreg <= (unsigned int)kSmpCand) {
-            // ---- the region sorted by (logit desc, index asc), scanned to the cut
-            __syncthreads();
-            if (tid == 0) sm.ncand = 0u;
-            __syncthreads();
-            for (int i = tid; i < V; i += kSmpThreads) {
-                const float v = z[i];
-                int bin;
+        if (nreg <= (unsigned long long)kSmpCand) {
+            // ---- the region gathered in the first CTA, sorted by (logit desc,
+            // index asc) and scanned to the cut
+            const uint32_t cnt0 = smp_map(&sm.ncand, 0u);
+            smp_each(z, s0, s1, [&](int i, float v) {
+                    int bin;
                 if (smp_live(v, mx, rt, inv, bin) && in_region(v, bin)) {
-                    const unsigned int slot = atomicAdd(&sm.ncand, 1u);
+                    const unsigned int slot = smp_atom_add(cnt0, 1u);
                     if (slot < (unsigned int)kSmpCand)
-                        sm.cand[slot] = ((unsigned long long)(~smp_key(v)) << 32) | (unsigned int)i;
+                        smp_st64(smp_map(&sm.cand[slot], 0u),
+                                 ((unsigned long long)(~smp_key(v)) << 32) | (unsigned int)i);
                 }
-            }
-            __syncthreads();
-            const int n = (int)min(sm.ncand, (unsigned int)kSmpCand);
-            int np = 1;
-            while (np < n) np <<= 1;
-            for (int j = n + tid; j < np; j += kSmpThreads) sm.cand[j] = ~0ull;
-            __syncthreads();
-            for (int k = 2; k <= np; k <<= 1)   // bitonic sort, ascending
-                for (int jj = k >> 1; jj > 0; jj >>= 1) {
-                    for (int x = tid; x < np; x += kSmpThreads) {
-                        const int y = x ^ jj;
-                        if (y > x) {
-                            const unsigned long long p0 = sm.cand[x], p1 = sm.cand[y];
-                            if ((p0 > p1) == ((x & k) == 0)) {
-                                sm.cand[x] = p1;
-                                sm.cand[y] = p0;
+            });
+            smp_cluster_sync();
+            if (rank == 0) {
+                const int n = (int)min(sm.ncand, (unsigned int)kSmpCand);
+                int np = 1;
+                while (np < n) np <<= 1;
+                for (int j = n + tid; j < np; j += kSmpThreads) sm.cand[j] = ~0ull;
+                __syncthreads();
+                for (int k = 2; k <= np; k <<= 1)   // bitonic sort, ascending
+                    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                        for (int x = tid; x < np; x += kSmpThreads) {
+                            const int y = x ^ jj;
+                            if (y > x) {
+                                const unsigned long long p0 = sm.cand[x], p1 = sm.cand[y];
+                                if ((p0 > p1) == ((x & k) == 0)) {
+                                    sm.cand[x] = p1;
+                                    sm.cand[y] = p0;
+                                }
                             }
                         }
+                        __syncthreads();
                     }
-                    __syncthreads();
+                constexpr int E = kSmpCand / kSmpThreads;
+                unsigned long long qs[E], loc = 0ull;
+                uint32_t ks[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int j = tid * E + e;
+                    qs[e] = 0ull;
+                    ks[e] = 0u;
+                    if (j < n) {
+                        ks[e] = ~(uint32_t)(sm.cand[j] >> 32);
+                        int bin;
+                        qs[e] = smp_mass(smp_unkey(ks[e]), mx, rt, inv, bin);
+                    }
+                    loc += qs[e];
                 }
-            constexpr int E = kSmpCand / kSmpThreads;
-            unsigned long long qs[E], loc = 0ull;
-            uint32_t ks[E];
+                unsigned long long tot;
+                const unsigned long long pre = smp_scan(loc, sm, tot);
+                // the first entry whose inclusive cumulative mass reaches `need`
+                unsigned long long run = pre;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int j = tid * E + e;
-                qs[e] = 0ull;
-                ks[e] = 0u;
-                if (j < n) {
-                    ks[e] = ~(uint32_t)(sm.cand[j] >> 32);
-                    int bin;
-                    qs[e] = smp_mass(smp_unkey(ks[e]), mx, rt, inv, bin);
+                for (int e = 0; e < E; ++e) {
+                    const int j = tid * E + e;
+                    if (j < n && run < need && run + qs[e] >= need) sm.ibcast[1] = j;
+                    run += qs[e];
                 }
-                loc += qs[e];
-            }
-            unsigned long long tot;
-            const unsigned long long pre = smp_scan(loc, sm, tot);
-            // the first entry whose inclusive cumulative mass reaches `need`
-            unsigned long long run = pre;
+                __syncthreads();
+                const uint32_t tk = ~(uint32_t)(sm.cand[sm.ibcast[1]] >> 32);
+                // the first entry with that logit, and the region's mass before it
+                run = pre;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int j = tid * E + e;
-                if (j < n && run < need && run + qs[e] >= need) sm.ibcast[1] = j;
-                run += qs[e];
+                for (int e = 0; e < E; ++e) {
+                    const int j = tid * E + e;
+                    if (j < n && ks[e] == tk && (j == 0 || ~(uint32_t)(sm.cand[j - 1] >> 32) != tk))
+                        sm.bcast[1] = run;
+                    run += qs[e];
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    sm.xch[8] = tk;
+                    sm.xch[9] = sm.bcast[1];
+                }
             }
-            __syncthreads();
-            tkey = ~(uint32_t)(sm.cand[sm.ibcast[1]] >> 32);
-            // the first entry with that logit, and the region's mass before it
-            run = pre;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int j = tid * E + e;
-                if (j < n && ks[e] == tkey && (j == 0 || ~(uint32_t)(sm.cand[j - 1] >> 32) != tkey))
-                    sm.bcast[1] = run;
-                run += qs[e];
-            }
-            __syncthreads();
-            mass_gt = base + sm.bcast[1];
+            smp_cluster_sync();
+            tkey = (uint32_t)smp_ld64(smp_map(&sm.xch[8], 0u));
+            mass_gt = base + smp_ld64(smp_map(&sm.xch[9], 0u));
         } else {
             // ---- a region of few repeated logit values: bisection over its keys for
             // the largest K with mass(region, key >= K) >= need
             unsigned long long lo = rlo, hi = (unsigned long long)rhi + 1ull, m_hi = 0ull;
+            int it = 0;
             while (hi - lo > 1ull) {
                 const unsigned long long mid = (lo + hi) >> 1;
                 unsigned long long part = 0ull;
-                for (int i = tid; i < V; i += kSmpThreads) {
-                    const float v = z[i];
-                    int bin;
+                smp_each(z, s0, s1, [&](int i, float v) {
+                            int bin;
                     const unsigned long long q = smp_mass(v, mx, rt, inv, bin);
                     if (q && in_region(v, bin) && (unsigned long long)smp_key(v) >= mid) part += q;
-                }
-                const unsigned long long mm = smp_sum(part, sm);
+                });
+                unsigned long long cta;
+                smp_scan(part, sm, cta);
+                unsigned long long mm;
+                smp_cluster_scan(cta, 10 + (it & 1), sm, rank, mm);
                 if (mm >= need) {
                     lo = mid;
                 } else {
                     hi = mid;
                     m_hi = mm;
                 }
+                ++it;
             }
             tkey = (uint32_t)lo;
             mass_gt = base + m_hi;
@@ -428,13 +586,13 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs
     // tokens with logit t* taken in index order: the fewest that reach the target
     const unsigned long long kties = (target - mass_gt + qt - 1ull) / qt;
 
-    // ---- 4. inverse cumulative mass over the nucleus in vocabulary order
-    const int chunk = (V + kSmpThreads - 1) / kSmpThreads;
-    const int c0 = min(V, tid * chunk), c1 = min(V, c0 + chunk);
+    // ---- inverse cumulative mass over the nucleus in vocabulary order: this
+    // thread's contiguous chunk of the slice, offsets by block and cluster scans
+    const int chunk = (s1 - s0 + kSmpThreads - 1) / kSmpThreads;
+    const int c0 = min(s1, s0 + tid * chunk), c1 = min(s1, c0 + chunk);
     unsigned long long gt = 0ull, nt = 0ull;
-    for (int i = c0; i < c1; ++i) {
-        const float v = z[i];
-        if (!(v == v)) continue;
+    smp_chunk(z, c0, c1, [&](int i, float v) {
+        if (!(v == v)) return;
         const uint32_t k = smp_key(v);
         if (k > tkey) {
             int bin;
@@ -442,14 +600,14 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs
         } else if (k == tkey) {
             ++nt;
         }
-    }
-    unsigned long long ntot;
-    const unsigned long long tie0 = smp_scan(nt, sm, ntot);   // ties before this chunk
-    const unsigned long long inc =
-        tie0 >= kties ? 0ull : (kties - tie0 < nt ? kties - tie0 : nt);
+    });
+    unsigned long long tie_cta, tie_all, mass_cta, Mn;
+    const unsigned long long tie_in = smp_scan(nt, sm, tie_cta);
+    const unsigned long long tie0 = smp_cluster_scan(tie_cta, 12, sm, rank, tie_all) + tie_in;
+    const unsigned long long inc = tie0 >= kties ? 0ull : (kties - tie0 < nt ? kties - tie0 : nt);
     const unsigned long long mym = gt + inc * qt;
-    unsigned long long Mn;
-    const unsigned long long start = smp_scan(mym, sm, Mn);   // nucleus mass before this chunk
+    const unsigned long long m_in = smp_scan(mym, sm, mass_cta);
+    const unsigned long long start = smp_cluster_scan(mass_cta, 13, sm, rank, Mn) + m_in;
     unsigned long long s = (unsigned long long)floor((double)u * (double)Mn);
     if (s >= Mn) s = Mn - 1ull;
     if (start <= s && s < start + mym) {
@@ -475,11 +633,12 @@ __global__ void __launch_bounds__(kSmpThreads, 1) sample_kernel(const SampleArgs
         }
         a.out[b] = tok;
     }
+    smp_cluster_sync();   // no CTA leaves while a peer may still read its shared memory
 }
 
 cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
-    if (a.V <= 0 || a.ld < a.V) return cudaErrorInvalidValue;
+    if (a.V <= 0 || a.ld < a.V || a.B > 65535) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -487,7 +646,21 @@ cudaError_t launch_sample(const SampleArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl_smem(sample_kernel, dim3(a.B), dim3(kSmpThreads), sizeof(SmpSmem), s, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kSmpCluster, (unsigned)a.B);
+    cfg.blockDim = dim3(kSmpThreads);
+    cfg.dynamicSmemBytes = sizeof(SmpSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kSmpCluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sample_kernel, a);
 }
 
 }  // namespace bloom

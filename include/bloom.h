@@ -371,9 +371,10 @@ bloom_status bloom_op_attn_decode(const void *q, const void *k_cache, const void
  * top_p >= 1 or NaN: every token with non-zero mass; top_p <= 0: the most
  * probable token; u < 0 or NaN counts as 0, u >= 1 takes the last nucleus
  * token.  Masses are 2^-40 fixed point of float32 exp, summed in 64-bit
- * integers: the result does not depend on summation order.  NaN logits take no
- * part.  One CTA of 1024 threads per row; BLOOM_E_INVALID for null pointers,
- * B outside 1..65535, V < 1 or ld < V. */
+ * integers: the result does not depend on summation order.  NaN logits, and
+ * logits more than 27 temperature units below the maximum (mass below 2^-38
+ * of the maximum's), take no part.  One cluster of 8 CTAs per row;
+ * BLOOM_E_INVALID for null pointers, B outside 1..65535, V < 1 or ld < V. */
 bloom_status bloom_op_sample(const float *logits, int32_t B, int32_t V, int64_t ld,
                              const float *temperature, const float *top_p, const float *u,
                              int32_t *out_tokens, void *stream);
