@@ -502,6 +502,39 @@ def sampling_extra(gm, sh, B, T, S, ids_d, mask_d, dev, stream, bg, hbm):
     return line
 
 
+def offload_extra(gm, sh, B, T, S, ids_d, mask_d, dev, stream):
+    """Decode steps with the K / V of the upper half of the layers in page-locked
+    host memory (read and written by the kernels over the host link) against
+    the same steps with the whole cache in HBM.  The KV bytes of the offloaded
+    layers over the added time give the bandwidth the host link delivered."""
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    n = min(20, S - T - 1)
+    half = sh.n_layer // 2
+    res = {}
+    for name, off in (("hbm", None), ("offloaded", half)):
+        kv = gm.new_kv(B, S, offload_from=off)
+        gm.prefill(kv, ids_d, mask_d, out_tokens=tok)
+        for _ in range(2):
+            gm.decode_step(kv, tok, tok)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n - 2):
+            gm.decode_step(kv, tok, tok)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = a.elapsed_time(b) / (n - 2)
+        del kv
+    keys = T + 2 + (n - 2) // 2     # mean keys per step of the timed steps
+    kv_bytes = (sh.n_layer - half) * B * 2 * keys * sh.hidden * 2
+    extra_ms = res["offloaded"] - res["hbm"]
+    return {"workload": f"{sh.name}: B {B}, K / V of layers {half}..{sh.n_layer - 1} in host memory",
+            "decode_step_ms_hbm": res["hbm"], "decode_step_ms_offloaded": res["offloaded"],
+            "offloaded_kv_bytes_per_step": kv_bytes,
+            "host_link_gbs": kv_bytes / (extra_ms / 1e3) / 1e9 if extra_ms > 0 else None}
+
+
 def op_sample_line(lg, temps, tops, u, dev, stream, bg, hbm, reps: int = 20):
     """The sampling kernel alone on these logits (CUDA events); its bytes are
     one read of the logits plus the per-row parameters and tokens."""
@@ -643,6 +676,7 @@ def run_ours(args, sh):
     if series:
         extras["decode_by_batch"] = decode_series(gm, sh, series, dev, stream, hbm)
         extras["sampling"] = sampling_extra(gm, sh, B, T, S, ids_d, mask_d, dev, stream, bg, hbm)
+        extras["kv_offload"] = offload_extra(gm, sh, B, T, S, ids_d, mask_d, dev, stream)
     gm.close()
     del gm, kv
     torch.cuda.synchronize(dev)

@@ -68,13 +68,18 @@ MAX_BATCH = 256
 
 class KVC(C.Structure):
     _fields_ = [("buf", P), ("bytes", C.c_size_t), ("batch", I32), ("max_seq", I32),
-                ("len", I32), ("row_len", I32 * MAX_BATCH), ("row_active", C.c_uint8 * MAX_BATCH)]
+                ("len", I32), ("row_len", I32 * MAX_BATCH), ("row_active", C.c_uint8 * MAX_BATCH),
+                ("host_buf", P), ("host_bytes", C.c_size_t), ("offload_from", I32)]
 
 
 _SIGS = {
     "bloom_kv_bytes": (C.c_size_t, [C.POINTER(Config), I32, I32]),
     "bloom_create": (I32, [C.POINTER(Config), C.POINTER(WeightsC), C.POINTER(P)]),
     "bloom_kv_init": (I32, [P, C.POINTER(KVC), P, C.c_size_t, I32, I32, P]),
+    "bloom_kv_bytes_offload": (I32, [C.POINTER(Config), I32, I32, I32, C.POINTER(C.c_size_t),
+                                     C.POINTER(C.c_size_t)]),
+    "bloom_kv_init_offload": (I32, [P, C.POINTER(KVC), P, C.c_size_t, P, C.c_size_t, I32, I32, I32,
+                                    P]),
     "bloom_prefill": (I32, [P, C.POINTER(KVC), P, P, I32, I32, P, P, P]),
     "bloom_decode_step": (I32, [P, C.POINTER(KVC), P, P, P, P]),
     "bloom_decode_step_sampled": (I32, [P, C.POINTER(KVC), P, P, P, P, P, P, P]),
@@ -135,18 +140,38 @@ def _stream(stream=None):
 
 
 class KV:
-    """A caller-owned KV cache (one device byte buffer) and its descriptor."""
+    """A caller-owned KV cache (one device byte buffer) and its descriptor;
+    with offload_from < n_layer the K and V of layers [offload_from, n_layer)
+    live in a second, page-locked host buffer the kernels read directly."""
 
-    def __init__(self, model: "Model", batch: int, max_seq: int, stream=None):
-        n = lib().bloom_kv_bytes(C.byref(model.cfg), batch, max_seq)
-        if n == 0:
-            raise BloomError(1, "bloom_kv_bytes rejected the arguments")
+    def __init__(self, model: "Model", batch: int, max_seq: int, stream=None,
+                 offload_from: Optional[int] = None):
+        self.offload_from = model.n_layer if offload_from is None else int(offload_from)
+        self.host = None
+        if self.offload_from >= model.n_layer:
+            n = lib().bloom_kv_bytes(C.byref(model.cfg), batch, max_seq)
+            if n == 0:
+                raise BloomError(1, "bloom_kv_bytes rejected the arguments")
+            hn = 0
+        else:
+            dn, hb = C.c_size_t(), C.c_size_t()
+            check(lib().bloom_kv_bytes_offload(C.byref(model.cfg), batch, max_seq,
+                                               self.offload_from, C.byref(dn), C.byref(hb)))
+            n, hn = dn.value, hb.value
         self.buf = torch.empty(n + 256, dtype=torch.uint8, device=model.device)
         off = (-self.buf.data_ptr()) % 256
         self.view = self.buf[off:off + n]
         self.c = KVC()
-        check(lib().bloom_kv_init(model.h, C.byref(self.c), P(self.view.data_ptr()), n, batch,
-                                  max_seq, _stream(stream)))
+        if hn == 0:
+            check(lib().bloom_kv_init(model.h, C.byref(self.c), P(self.view.data_ptr()), n, batch,
+                                      max_seq, _stream(stream)))
+        else:
+            self.host = torch.empty(hn + 256, dtype=torch.uint8, pin_memory=True)
+            hoff = (-self.host.data_ptr()) % 256
+            self.host_view = self.host[hoff:hoff + hn]
+            check(lib().bloom_kv_init_offload(model.h, C.byref(self.c), P(self.view.data_ptr()), n,
+                                              P(self.host_view.data_ptr()), hn, batch, max_seq,
+                                              self.offload_from, _stream(stream)))
 
     @property
     def len(self) -> int:
@@ -172,14 +197,20 @@ class KV:
         off_np = al(off_act + 4 * B)
         off_pos = al(off_np + 4 * B)
         layer = B * sh.n_head * S * sh.head_dim * 2
+        nd = min(self.offload_from, model.n_layer)   # layers in the device buffer
         off_k = al(off_pos + 4 * B * S)
-        off_v = al(off_k + layer * model.n_layer)
+        off_v = al(off_k + layer * nd)
         v = self.view
         i32 = lambda a, n: v[a:a + 4 * n].view(torch.int32)
-        bf = lambda a: v[a:a + layer * model.n_layer].view(torch.bfloat16).view(
-            model.n_layer, B, sh.n_head, S, sh.head_dim)
-        return {"len": i32(off_len, B), "active": i32(off_act, B), "next_pos": i32(off_np, B),
-                "pos": i32(off_pos, B * S).view(B, S), "k": bf(off_k), "v": bf(off_v)}
+        bf = lambda buf, a, nl: buf[a:a + layer * nl].view(torch.bfloat16).view(
+            nl, B, sh.n_head, S, sh.head_dim)
+        out = {"len": i32(off_len, B), "active": i32(off_act, B), "next_pos": i32(off_np, B),
+               "pos": i32(off_pos, B * S).view(B, S), "k": bf(v, off_k, nd), "v": bf(v, off_v, nd)}
+        if self.host is not None:
+            nh = model.n_layer - nd
+            out["k_host"] = bf(self.host_view, 0, nh)
+            out["v_host"] = bf(self.host_view, al(layer * nh), nh)
+        return out
 
 
 class Model:
@@ -227,8 +258,8 @@ class Model:
     def decode_launches(self, batch: int) -> int:
         return lib().bloom_decode_launches(self.h, batch)
 
-    def new_kv(self, batch: int, max_seq: int, stream=None) -> KV:
-        return KV(self, batch, max_seq, stream)
+    def new_kv(self, batch: int, max_seq: int, stream=None, offload_from: Optional[int] = None) -> KV:
+        return KV(self, batch, max_seq, stream, offload_from)
 
     def prefill(self, kv: KV, tokens, mask, out_tokens=None, logits=None, stream=None):
         B, T = tokens.shape

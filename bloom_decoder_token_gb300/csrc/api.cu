@@ -69,7 +69,10 @@ struct KvLayout {
 
 // [256-byte header][len int32[B]][active int32[B]][next_pos int32[B]]
 // [pos int32[B][S]][K bf16[L][B][n][S][d]][V ...], every region 256-byte aligned.
-static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq) {
+// hbm_layers: the layers whose K and V live in this buffer (the first ones);
+// the rest live in the host buffer of an offloaded cache (kv_host_layout).
+static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq, int hbm_layers = -1) {
+    if (hbm_layers < 0) hbm_layers = c.n_layer;
     KvLayout L;
     const size_t d = (size_t)(c.hidden / c.n_head);
     size_t off = 256;
@@ -83,11 +86,25 @@ static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq) {
     off = align256(off + 4 * (size_t)batch * max_seq);
     L.layer = (size_t)batch * c.n_head * max_seq * d * 2;
     L.k = off;
-    off = align256(off + L.layer * c.n_layer);
+    off = align256(off + L.layer * hbm_layers);
     L.v = off;
-    off = align256(off + L.layer * c.n_layer);
+    off = align256(off + L.layer * hbm_layers);
     L.total = off;
     return L;
+}
+
+// Host part of an offloaded cache: K then V of layers [offload_from, n_layer).
+struct KvHostLayout {
+    size_t k, v, total;
+};
+static KvHostLayout kv_host_layout(const bloom_config &c, int batch, int max_seq, int offload_from) {
+    const KvLayout L = kv_layout(c, batch, max_seq);
+    const size_t n = (size_t)(c.n_layer - offload_from);
+    KvHostLayout H;
+    H.k = 0;
+    H.v = align256(L.layer * n);
+    H.total = align256(H.v + L.layer * n);
+    return H;
 }
 
 // ----------------------------------------------------------------- model
@@ -97,6 +114,9 @@ static KvLayout kv_layout(const bloom_config &c, int batch, int max_seq) {
 struct GraphEntry {
     void *kvbuf;
     size_t kvbytes;
+    void *hostbuf;      // offloaded layers' K / V (null: none)
+    size_t hostbytes;
+    int offload_from;
     int B, max_seq;
     const void *next;
     void *out;
@@ -200,6 +220,21 @@ static bloom_status validate_config(const bloom_config *c) {
 extern "C" size_t bloom_kv_bytes(const bloom_config *cfg, int32_t batch, int32_t max_seq) {
     if (validate_config(cfg) != BLOOM_OK || batch < 1 || max_seq < 1) return 0;
     return kv_layout(*cfg, batch, max_seq).total;
+}
+
+extern "C" bloom_status bloom_kv_bytes_offload(const bloom_config *cfg, int32_t batch,
+                                               int32_t max_seq, int32_t offload_from,
+                                               size_t *device_bytes, size_t *host_bytes) {
+    bloom_status st = validate_config(cfg);
+    if (st) return st;
+    if (!device_bytes || !host_bytes) return fail(BLOOM_E_INVALID, "null argument");
+    if (batch < 1 || max_seq < 1 || offload_from < 0 || offload_from > cfg->n_layer)
+        return fail(BLOOM_E_INVALID, "batch %d max_seq %d offload_from %d", batch, max_seq,
+                    offload_from);
+    *device_bytes = kv_layout(*cfg, batch, max_seq, offload_from).total;
+    *host_bytes = offload_from < cfg->n_layer
+                      ? kv_host_layout(*cfg, batch, max_seq, offload_from).total : 0;
+    return BLOOM_OK;
 }
 
 extern "C" bloom_status bloom_destroy(bloom_model *m) {
@@ -378,29 +413,65 @@ static bloom_status check_kv(const bloom_model *m, const bloom_kv *kv) {
     if (kv->batch < 1 || kv->batch > m->cfg.max_batch)
         return fail(BLOOM_E_CAPACITY, "kv batch %d above max_batch %d", kv->batch, m->cfg.max_batch);
     if (kv->max_seq < 1) return fail(BLOOM_E_INVALID, "kv max_seq %d", kv->max_seq);
-    if (kv->bytes < kv_layout(m->cfg, kv->batch, kv->max_seq).total)
+    if (kv->offload_from < 0 || kv->offload_from > m->cfg.n_layer ||
+        (kv->offload_from < m->cfg.n_layer && !kv->host_buf))
+        return fail(BLOOM_E_INVALID, "kv offload_from %d / host buffer", kv->offload_from);
+    if (kv->bytes < kv_layout(m->cfg, kv->batch, kv->max_seq, kv->offload_from).total)
         return fail(BLOOM_E_INVALID, "kv buffer too small");
+    if (kv->offload_from < m->cfg.n_layer &&
+        kv->host_bytes < kv_host_layout(m->cfg, kv->batch, kv->max_seq, kv->offload_from).total)
+        return fail(BLOOM_E_INVALID, "kv host buffer too small");
     return BLOOM_OK;
 }
 
-extern "C" bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
-                                      int32_t batch, int32_t max_seq, void *stream) {
+static bool ranges_overlap(const void *a, size_t an, const void *b, size_t bn) {
+    if (!a || !b) return false;
+    const char *a0 = (const char *)a, *b0 = (const char *)b;
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+static bloom_status kv_init_impl(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
+                                 void *host_buf, size_t host_bytes, int32_t batch,
+                                 int32_t max_seq, int32_t offload_from, void *stream) {
     if (!m || !kv || !buf) return fail(BLOOM_E_INVALID, "null argument");
     if (((uintptr_t)buf & 255u) != 0) return fail(BLOOM_E_INVALID, "kv buffer not 256-byte aligned");
     if (batch < 1 || batch > m->cfg.max_batch)
         return fail(BLOOM_E_CAPACITY, "batch %d outside 1..max_batch %d", batch, m->cfg.max_batch);
     if (max_seq < 1 || max_seq > m->cfg.max_seq)
         return fail(BLOOM_E_CAPACITY, "max_seq %d outside 1..%d", max_seq, m->cfg.max_seq);
-    const KvLayout L = kv_layout(m->cfg, batch, max_seq);
+    if (offload_from < 0 || offload_from > m->cfg.n_layer)
+        return fail(BLOOM_E_INVALID, "offload_from %d outside 0..%d", offload_from, m->cfg.n_layer);
+    const KvLayout L = kv_layout(m->cfg, batch, max_seq, offload_from);
     if (bytes < L.total) return fail(BLOOM_E_INVALID, "kv buffer %zu < %zu bytes", bytes, L.total);
+    if (offload_from < m->cfg.n_layer) {
+        if (!host_buf) return fail(BLOOM_E_INVALID, "null host buffer");
+        if (((uintptr_t)host_buf & 255u) != 0)
+            return fail(BLOOM_E_INVALID, "kv host buffer not 256-byte aligned");
+        const KvHostLayout H = kv_host_layout(m->cfg, batch, max_seq, offload_from);
+        if (host_bytes < H.total)
+            return fail(BLOOM_E_INVALID, "kv host buffer %zu < %zu bytes", host_bytes, H.total);
+        // the kernels dereference it directly: page-locked host memory that the
+        // device addresses with the same pointer
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, host_buf) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
+            pa.devicePointer != host_buf) {
+            cudaGetLastError();
+            return fail(BLOOM_E_INVALID, "kv host buffer is not page-locked host memory the "
+                        "device maps at the same address");
+        }
+    } else {
+        host_buf = nullptr;
+        host_bytes = 0;
+    }
     cudaStream_t s = (cudaStream_t)stream;
-    // graphs captured on a cache that overlaps this buffer describe a layout that
-    // no longer exists (the caller re-bound or re-allocated the memory)
+    // graphs captured on a cache that overlaps these buffers describe a layout
+    // that no longer exists (the caller re-bound or re-allocated the memory)
     for (size_t i = 0; i < m->graphs.size();) {
         const GraphEntry &g = m->graphs[i];
-        const char *a0 = (const char *)g.kvbuf, *a1 = a0 + g.kvbytes;
-        const char *b0 = (const char *)buf, *b1 = b0 + bytes;
-        if (a0 < b1 && b0 < a1) {
+        if (ranges_overlap(g.kvbuf, g.kvbytes, buf, bytes) ||
+            ranges_overlap(g.hostbuf, g.hostbytes, host_buf, host_bytes) ||
+            ranges_overlap(g.hostbuf, g.hostbytes, buf, bytes) ||
+            ranges_overlap(g.kvbuf, g.kvbytes, host_buf, host_bytes)) {
             cudaGraphExecDestroy(g.exec);
             m->graphs.erase(m->graphs.begin() + (long)i);
         } else {
@@ -418,7 +489,23 @@ extern "C" bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, s
         kv->row_len[b] = 0;
         kv->row_active[b] = 0;
     }
+    kv->host_buf = host_buf;
+    kv->host_bytes = host_bytes;
+    kv->offload_from = offload_from;
     return BLOOM_OK;
+}
+
+extern "C" bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
+                                      int32_t batch, int32_t max_seq, void *stream) {
+    return kv_init_impl(m, kv, buf, bytes, nullptr, 0, batch, max_seq, m ? m->cfg.n_layer : 0,
+                        stream);
+}
+
+extern "C" bloom_status bloom_kv_init_offload(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
+                                              void *host_buf, size_t host_bytes, int32_t batch,
+                                              int32_t max_seq, int32_t offload_from, void *stream) {
+    return kv_init_impl(m, kv, buf, bytes, host_buf, host_bytes, batch, max_seq, offload_from,
+                        stream);
 }
 
 // Host mirror of the cache's per-row state: kv->len = the longest active row.
@@ -457,11 +544,19 @@ static void kv_mirror_step(bloom_kv *kv) {
 // pointers into a kv buffer
 struct KvPtrs {
     int *len, *active, *next_pos, *pos;
-    uint16_t *k, *v;
+    uint16_t *k, *v;              // layers [0, offload_from)
+    uint16_t *k_host, *v_host;    // layers [offload_from, n_layer), in host memory
+    int offload_from;
     size_t layer_elems;
+    uint16_t *k_layer(int l) const {
+        return l < offload_from ? k + layer_elems * l : k_host + layer_elems * (l - offload_from);
+    }
+    uint16_t *v_layer(int l) const {
+        return l < offload_from ? v + layer_elems * l : v_host + layer_elems * (l - offload_from);
+    }
 };
 static KvPtrs kv_ptrs(const bloom_model *m, const bloom_kv *kv) {
-    const KvLayout L = kv_layout(m->cfg, kv->batch, kv->max_seq);
+    const KvLayout L = kv_layout(m->cfg, kv->batch, kv->max_seq, kv->offload_from);
     char *b = (char *)kv->buf;
     KvPtrs p;
     p.len = (int *)(b + L.len);
@@ -470,6 +565,14 @@ static KvPtrs kv_ptrs(const bloom_model *m, const bloom_kv *kv) {
     p.pos = (int *)(b + L.pos);
     p.k = (uint16_t *)(b + L.k);
     p.v = (uint16_t *)(b + L.v);
+    p.offload_from = kv->offload_from;
+    p.k_host = p.v_host = nullptr;
+    if (kv->offload_from < m->cfg.n_layer) {
+        const KvHostLayout H = kv_host_layout(m->cfg, kv->batch, kv->max_seq, kv->offload_from);
+        char *h = (char *)kv->host_buf;
+        p.k_host = (uint16_t *)(h + H.k);
+        p.v_host = (uint16_t *)(h + H.v);
+    }
     p.layer_elems = L.layer / 2;
     return p;
 }
@@ -643,8 +746,8 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
     cudaError_t e;
     LinearArgs q = lin_args(L.qkv, i8, m->a, M, 3 * h, h, EPI_QKV);
     q.q_out = m->q;
-    q.k_cache = kp.k + kp.layer_elems * l;
-    q.v_cache = kp.v + kp.layer_elems * l;
+    q.k_cache = kp.k_layer(l);
+    q.v_cache = kp.v_layer(l);
     q.len_ptr = kp.len;
     q.active = kp.active;
     q.T = T;
@@ -885,9 +988,10 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
     } else {
         cudaGraphExec_t exec = nullptr;
         for (auto &g : m->graphs)
-            if (g.kvbuf == kv->buf && g.kvbytes == kv->bytes && g.B == kv->batch &&
-                g.max_seq == kv->max_seq && g.next == next_tokens && g.out == out_tokens &&
-                g.logits == out_logits) {
+            if (g.kvbuf == kv->buf && g.kvbytes == kv->bytes && g.hostbuf == kv->host_buf &&
+                g.hostbytes == kv->host_bytes && g.offload_from == kv->offload_from &&
+                g.B == kv->batch && g.max_seq == kv->max_seq && g.next == next_tokens &&
+                g.out == out_tokens && g.logits == out_logits) {
                 exec = g.exec;
                 break;
             }
@@ -908,7 +1012,8 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
                 cudaGraphExecDestroy(m->graphs.front().exec);
                 m->graphs.erase(m->graphs.begin());
             }
-            m->graphs.push_back({kv->buf, kv->bytes, kv->batch, kv->max_seq, next_tokens,
+            m->graphs.push_back({kv->buf, kv->bytes, kv->host_buf, kv->host_bytes,
+                                 kv->offload_from, kv->batch, kv->max_seq, next_tokens,
                                  out_tokens, out_logits, exec});
         }
         CK(cudaGraphLaunch(exec, s));

@@ -137,6 +137,9 @@ typedef struct {
     int32_t len;                              /* longest active row */
     int32_t row_len[BLOOM_MAX_BATCH];         /* slots filled, per row */
     uint8_t row_active[BLOOM_MAX_BATCH];      /* 1: the row decodes */
+    void   *host_buf;                         /* K / V of layers >= offload_from (NULL: none) */
+    size_t  host_bytes;
+    int32_t offload_from;                     /* first layer kept in host_buf (n_layer: none) */
 } bloom_kv;
 
 /* Bytes a cache for `batch` sequences of `max_seq` slots needs (0 on bad args). */
@@ -154,6 +157,28 @@ bloom_status bloom_create(const bloom_config *cfg, const bloom_weights *w, bloom
  * cache and fill *kv: every row empty and idle, every slot a pad. */
 bloom_status bloom_kv_init(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
                            int32_t batch, int32_t max_seq, void *stream);
+
+/* KV offload to host memory ("DeepSpeed Inference", IV.C.2 Offloading
+ * Activations to CPU Memory: cached keys and values beyond what the GPU
+ * should hold go to CPU memory, so that larger batches fit; IV.C.3 overlaps
+ * the PCIe traffic with compute.  On GB300 the Grace memory is read and
+ * written by the kernels themselves over NVLink-C2C, with no copies to
+ * schedule): the K and V of layers [offload_from, n_layer) live in host_buf,
+ * everything else in buf.  Sizes of both parts (offload_from = n_layer:
+ * host_bytes = 0, device_bytes = bloom_kv_bytes).  BLOOM_E_INVALID on bad
+ * arguments. */
+bloom_status bloom_kv_bytes_offload(const bloom_config *cfg, int32_t batch, int32_t max_seq,
+                                    int32_t offload_from, size_t *device_bytes,
+                                    size_t *host_bytes);
+
+/* bloom_kv_init with layers [offload_from, n_layer) in host_buf: page-locked
+ * host memory (cudaHostAlloc / cudaMallocHost, 256-byte aligned) that the
+ * device addresses with the same pointer -- checked, else BLOOM_E_INVALID.
+ * The caller owns both buffers.  Decode and prefill kernels read and write the
+ * offloaded layers' cache directly (zero-copy), at the host link's bandwidth. */
+bloom_status bloom_kv_init_offload(bloom_model *m, bloom_kv *kv, void *buf, size_t bytes,
+                                   void *host_buf, size_t host_bytes, int32_t batch,
+                                   int32_t max_seq, int32_t offload_from, void *stream);
 
 /* Prefill: run the B x T padded prompts (tokens int32 [B][T], mask uint8 [B][T],
  * 1 = token, 0 = pad; each row needs one token), write K,V of slots [0,T),
