@@ -1253,7 +1253,6 @@ extern "C" bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, in
         !gemm_make_map(mx.b, x, M, K, gemm_box_rows_x()) ||
         !gemm_make_map(mw.b, lin->w, N, K, gemm_box_rows_w()))
         return fail(BLOOM_E_UNSUPPORTED, "TMA descriptors could not be encoded");
-    CK(gemm_prepare());
     LinearArgs a = lin_args(*lin, 0, (const uint16_t *)x, M, N, K, epilogue);
     a.out = (uint16_t *)y;
     CK(launch_gemm_tc(mx.b, mw.b, a, (cudaStream_t)stream));

@@ -43,14 +43,15 @@ constexpr int kTcBBytes = kTcBN * kTcBK * 2;     // 32 KB
 constexpr int kTcStageBytes = kTcABytes + kTcBBytes;
 constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 1024;   // + 1 KB alignment slack
 // Epilogue of 32 consecutive features [nb, nb + 32) of token row m (v = the
-// accumulators); features >= a.N are dropped.
+// accumulators; bias: those features' bias in shared memory, or null);
+// features >= a.N are dropped.
 template <int EPI>
-__device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[32], int m, int nb) {
+__device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[32], int m, int nb,
+                                               const uint16_t *bias) {
     const int nv = min(32, a.N - nb);
-    if (a.bias) {
+    if (bias) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < nv) v[i] += bf2f(a.bias[nb + i]);
+        for (int i = 0; i < 32; ++i) v[i] += bf2f(bias[i]);
     }
     if constexpr (EPI == EPI_GELU) {
 #pragma unroll
@@ -145,6 +146,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     __shared__ uint64_t full[kTcStages], empty[kTcStages], acc_full[2], acc_empty[2], drained;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
+    __shared__ uint16_t s_bias[4][kTcBN];   // the tile's bias, one copy per epilogue warp
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nkb = (a.K + kTcBK - 1) / kTcBK;
@@ -267,6 +269,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             int m0, n0;
             tc_tile_coords(t, tiles_m, tiles_n, m0, n0);
             const int m = m0 + row;
+            // the tile's bias into this warp's copy while the main loop runs: eight
+            // independent loads per lane instead of a round trip per 32-feature chunk
+            if (a.bias) {
+                __syncwarp();   // the previous tile's reads are done
+#pragma unroll
+                for (int j = 0; j < kTcBN / 32; ++j) {
+                    const int f = lane * (kTcBN / 32) + j;
+                    s_bias[quarter][f] = n0 + f < a.N ? a.bias[n0 + f] : (uint16_t)0;
+                }
+                __syncwarp();
+            }
             // longer limit than the MMA issuer's, so that its commits arrive first
             const bool ok = tc_mbar_wait(&acc_full[b], (uint32_t)((lt >> 1) & 1),
                                          3 * (a.wait_ns ? a.wait_ns : kTcWaitNs));
@@ -282,7 +295,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int c = 0; c < kTcBN; c += 32) {
                 float v[32];
                 tc_ld32(acc + (uint32_t)c, v);   // whole warp
-                if (store && n0 + c < a.N) tc_store_chunk<EPI>(a, v, m, n0 + c);
+                if (store && n0 + c < a.N)
+                    tc_store_chunk<EPI>(a, v, m, n0 + c, a.bias ? &s_bias[quarter][c] : nullptr);
             }
             // buffer b drained: the MMA issuer may start the tile after next in it
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
