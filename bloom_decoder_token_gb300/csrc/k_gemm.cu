@@ -47,7 +47,7 @@ constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 1024;   // + 1 KB
 // features >= a.N are dropped.
 template <int EPI>
 __device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[32], int m, int nb,
-                                               const uint16_t *bias) {
+                                               const uint16_t *bias, const float (&res)[32]) {
     const int nv = min(32, a.N - nb);
     if (bias) {
 #pragma unroll
@@ -58,21 +58,18 @@ __device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[3
         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
     }
     if constexpr (EPI == EPI_RESID32) {
+        // res: the residual of these features, loaded a chunk ahead (tc_load_res)
         float *o = a.out32 + (size_t)m * a.N + nb;
         if (nv == 32 && ((uintptr_t)o & 15u) == 0) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                float4 r = *reinterpret_cast<float4 *>(o + i);
-                r.x += v[i];
-                r.y += v[i + 1];
-                r.z += v[i + 2];
-                r.w += v[i + 3];
-                *reinterpret_cast<float4 *>(o + i) = r;
-            }
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(o + i) =
+                    make_float4(res[i] + v[i], res[i + 1] + v[i + 1], res[i + 2] + v[i + 2],
+                                res[i + 3] + v[i + 3]);
         } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                if (i < nv) o[i] += v[i];
+                if (i < nv) o[i] = res[i] + v[i];
         }
     } else {
         uint16_t *o;
@@ -116,6 +113,31 @@ __device__ __forceinline__ void tc_store_chunk(const LinearArgs &a, float (&v)[3
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 if (i < nv) o[i] = f2bf(v[i]);
+        }
+    }
+}
+
+// The float32 residual of features [nb, nb + 32) of row m (EPI_RESID32), for
+// the chunk after the one being stored: its loads overlap that chunk's work.
+template <int EPI>
+__device__ __forceinline__ void tc_load_res(const LinearArgs &a, float (&r)[32], int m, int nb,
+                                            bool live) {
+    if constexpr (EPI == EPI_RESID32) {
+        if (!live) return;
+        const int nv = min(32, a.N - nb);
+        const float *o = a.out32 + (size_t)m * a.N + nb;
+        if (nv == 32 && ((uintptr_t)o & 15u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(o + i);
+                r[i] = x.x;
+                r[i + 1] = x.y;
+                r[i + 2] = x.z;
+                r[i + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = i < nv ? o[i] : 0.f;
         }
     }
 }
@@ -291,12 +313,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const bool store = !*abort_flag && m < a.M;
             const uint32_t acc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kTcBN);
+            float res[32], res_next[32];
+            tc_load_res<EPI>(a, res, m, n0, store && n0 < a.N);
 #pragma unroll 1
             for (int c = 0; c < kTcBN; c += 32) {
                 float v[32];
                 tc_ld32(acc + (uint32_t)c, v);   // whole warp
+                const bool more = c + 32 < kTcBN;
+                tc_load_res<EPI>(a, res_next, m, n0 + c + 32, store && more && n0 + c + 32 < a.N);
                 if (store && n0 + c < a.N)
-                    tc_store_chunk<EPI>(a, v, m, n0 + c, a.bias ? &s_bias[quarter][c] : nullptr);
+                    tc_store_chunk<EPI>(a, v, m, n0 + c, a.bias ? &s_bias[quarter][c] : nullptr, res);
+                if constexpr (EPI == EPI_RESID32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) res[i] = res_next[i];
+                }
             }
             // buffer b drained: the MMA issuer may start the tile after next in it
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
