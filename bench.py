@@ -684,7 +684,7 @@ def run_ours(args, sh):
         del w
         torch.cuda.empty_cache()
         extras["int8_7b1"] = extra_stack("7b1int8", (1, 8, 32, 128), dev, args, bg, hbm)
-        extras["cfg_176b14"] = extra_stack("176b14", (1, 8, 32), dev, args, bg, hbm)
+        extras["cfg_176b14"] = extra_stack("176b14", (1, 8, 32, 128, 256), dev, args, bg, hbm)
         extras["prefill_176b14_4x2048"] = prefill_extra("176b14", 4, 2048, dev, args, bg)
         extras["prefill_7b1_128x16"] = prefill_extra("7b1", 128, 16, dev, args, bg)
 
