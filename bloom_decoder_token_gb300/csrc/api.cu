@@ -645,6 +645,7 @@ static GemvTcArgs tc_args(const bloom_model *m, const LinearArgs &a) {
     GemvTcArgs g;
     g.a = a;
     g.a.wait_ns = (unsigned long long)m->cfg.wait_us * 1000ull;
+    if (!g.a.err) g.a.err = m->err;   // an expired wait is reported by bloom_check_device
     g.splits = gemv_tc_splits(a.N, a.K, a.M, a.epi, m->num_sms, a.int8);
     return g;
 }
@@ -690,6 +691,7 @@ static cudaError_t run_linear(bloom_model *m, const LinearArgs &a, int l, int wm
     if (m->tc && a.T > 0 && a.M >= kTcMinM && !a.ln_x) {
         LinearArgs b = a;
         b.wait_ns = (unsigned long long)m->cfg.wait_us * 1000ull;
+        if (!b.err) b.err = m->err;
         e = launch_gemm_tc(m->xmaps[xmap].b, m->wmaps[(size_t)l * TC_PER_LAYER + wmap].b, b, s);
         kernel = BLOOM_KERNEL_GEMM_TC;
     } else if (use_tc_linear(m, a)) {
