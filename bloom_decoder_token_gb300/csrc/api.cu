@@ -18,6 +18,9 @@ using namespace bloom;
 
 namespace bloom {
 thread_local bool g_pdl = true;
+// Set while a decode step is captured into a graph: every kernel of an earlier
+// step, and of the calls before it, has finished when the graph starts.
+static thread_local bool g_capture = false;
 }
 
 // ----------------------------------------------------------------- errors
@@ -138,6 +141,7 @@ struct bloom_model {
     std::vector<bloom_layer_weights> layers;
     int dev = 0, num_sms = 0;
     int d = 0;
+    long long attn_resident = 0;   // attn_decode_resident_ctas
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *x = nullptr;           // float32 residual stream [max_tokens][h]
@@ -281,6 +285,8 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     m->d = h / cfg->n_head;
     cudaError_t e = cudaGetDevice(&m->dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->dev);
+    if (e == cudaSuccess && (m->d == 64 || m->d == 128))
+        m->attn_resident = attn_decode_resident_ctas(m->d, m->num_sms);
     if (e != cudaSuccess) {
         delete m;
         return fail(BLOOM_E_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
@@ -774,6 +780,8 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.d = d;
         at.max_seq = max_seq;
         at.splits = splits;
+        at.early = (g_capture && g_pdl) ? 1 : 0;
+        at.resident_ctas = m->attn_resident;
         at.scale = (float)(1.0 / sqrt((double)d));
         at.part = m->attn_part;
         at.ticket = m->attn_ticket;
@@ -1000,7 +1008,9 @@ extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const in
         if (!exec) {
             cudaGraph_t graph = nullptr;
             CK(cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal));
+            g_capture = true;
             cudaError_t e = enqueue_decode(m, kv, next_tokens, out_tokens, out_logits, m->cap);
+            g_capture = false;
             cudaError_t e2 = cudaStreamEndCapture(m->cap, &graph);
             if (e != cudaSuccess || e2 != cudaSuccess) {
                 if (graph) cudaGraphDestroy(graph);
@@ -1323,6 +1333,7 @@ extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
     a.max_seq = max_seq;
     a.splits = splits;
     a.scale = (float)(1.0 / sqrt((double)d));
+    a.resident_ctas = attn_decode_resident_ctas(d, device_sms());
     void *scratch = nullptr;
     const size_t part_bytes = align256((size_t)B * n_head * splits * (d + 2) * 4);
     const size_t bytes = part_bytes + (size_t)B * n_head * 4;

@@ -54,17 +54,23 @@ struct AttnSmem {
 
 // All NT threads of the block call it with the same (split, j, b).  Contains
 // barriers; the first one also protects `sm` from a previous call's readers.
+// It waits for the previous kernel itself (griddepcontrol.wait): with a.early
+// the length, the activity and the K / V / positions of the keys that earlier
+// steps cached (slots below the length) are read first, so that the first
+// round's loads overlap the QKV kernel that is still appending this step's key.
 template <int D, int NT>
 __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int split, int j, int b,
                                                   AttnSmem<D, NT> &sm) {
     constexpr int EPT = D / 8;             // elements per lane of an 8-lane group
     constexpr int NW = NT / 32;
     constexpr int NG = NT / 8;             // groups; a round covers kAttnKeysPerGroup * NG keys
+    constexpr int KPG = kAttnKeysPerGroup;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = tid >> 3, sub = tid & 7;
+    if (!a.early) griddep_wait();
     // keys [0, len] with the step's new one; an idle row appended none
-    const int nk = a.len_ptr ? min(a.len_ptr[b] + ((!a.active || a.active[b]) ? 1 : 0), a.max_seq)
-                             : min(a.len_host + 1, a.max_seq);
+    const int len = a.len_ptr ? a.len_ptr[b] : a.len_host;
+    const int nk = min(len + ((!a.len_ptr || !a.active || a.active[b]) ? 1 : 0), a.max_seq);
     int chunk = (nk + a.splits - 1) / a.splits;
     if (chunk < kAttnMinKeysPerSplit) chunk = kAttnMinKeysPerSplit;
     const int splits = nk > 0 ? (nk + chunk - 1) / chunk : 1;   // uniform over the blocks of (b, j)
@@ -78,6 +84,25 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
     const int *posb = a.pos + (size_t)b * a.max_seq;
     const float slope = a.slopes[j];
 
+    bool live[KPG], have[KPG];
+    int pk[KPG];
+    uint4 kv[KPG][EPT / 8], vv[KPG][EPT / 8];
+    auto load_key = [&](int u, int key) {
+        pk[u] = posb[key];
+#pragma unroll
+        for (int i = 0; i < EPT / 8; ++i) {
+            kv[u][i] = *reinterpret_cast<const uint4 *>(kbase + (size_t)key * D + 8 * i);
+            vv[u][i] = *reinterpret_cast<const uint4 *>(vbase + (size_t)key * D + 8 * i);
+        }
+    };
+#pragma unroll
+    for (int u = 0; u < KPG; ++u) {
+        const int key = k0 + u * NG + grp;   // round 0
+        have[u] = a.early && key < k1 && key < len;
+        if (have[u]) load_key(u, key);
+    }
+    if (a.early) griddep_wait();   // q, and the new key's K / V / position, come from this step
+
     float qf[EPT], acc[EPT];
     {
         const uint16_t *qp = a.q + bh * D + sub * EPT;
@@ -90,25 +115,14 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
         }
     }
     float m_run = -INFINITY, l_run = 0.f;
-    constexpr int KPG = kAttnKeysPerGroup;
     const int rounds = (k1 - k0 + KPG * NG - 1) / (KPG * NG);
     for (int r = 0; r < rounds; ++r) {
-        bool live[KPG];
-        int pk[KPG];
-        uint4 kv[KPG][EPT / 8], vv[KPG][EPT / 8];
 #pragma unroll
         for (int u = 0; u < KPG; ++u) {
             const int key = k0 + (r * KPG + u) * NG + grp;
             live[u] = key < k1;
-            pk[u] = -1;
-            if (live[u]) {
-                pk[u] = posb[key];
-#pragma unroll
-                for (int i = 0; i < EPT / 8; ++i) {
-                    kv[u][i] = *reinterpret_cast<const uint4 *>(kbase + (size_t)key * D + 8 * i);
-                    vv[u][i] = *reinterpret_cast<const uint4 *>(vbase + (size_t)key * D + 8 * i);
-                }
-            }
+            if (live[u] && !(r == 0 && have[u])) load_key(u, key);
+            if (!live[u]) pk[u] = -1;
         }
         float sc[KPG];
 #pragma unroll

@@ -20,20 +20,40 @@ constexpr int kAttnThreads = 128;
 
 // ---------------------------------------------------------------------------
 // Decode: one query per (sequence, head).  Grid (splits, n_head, B): each CTA
-// takes one contiguous key range (attn_decode_block).
+// takes one contiguous key range (attn_decode_block, which also waits for the
+// previous kernel).
 // ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnDecodeArgs a) {
+template <int D, int MINB>
+__global__ void __launch_bounds__(kAttnThreads, MINB) attn_decode_kernel(const AttnDecodeArgs a) {
     __shared__ AttnSmem<D, kAttnThreads> sm;
     griddep_launch();
-    griddep_wait();
     attn_decode_block<D, kAttnThreads>(a, blockIdx.x, blockIdx.y, blockIdx.z, sm);
+}
+
+// Two register budgets for d = 128: unbounded (about 105 registers, four CTAs an
+// SM) where the whole grid is resident at once, else capped for six CTAs an SM
+// (80 registers, no spills).  Measured on GB300 (7b1, 30 layers, decode step):
+// 1 / 8 sequences (128 / 512 CTAs) 3.081 / 2.988 ms unbounded vs 3.088 / 3.023
+// capped; 32 sequences (1024 CTAs) 3.495 vs 3.475; a cap of 64 registers (eight
+// CTAs an SM) spills and took 3.133 / 3.151 / 3.626 ms.
+constexpr int kAttnCappedMinBlocks = 6;
+
+int attn_decode_resident_ctas(int d, int num_sms) {
+    int per_sm = 0;
+    const cudaError_t e = d == 128
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<128, 1>, kAttnThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<64, 1>, kAttnThreads, 0);
+    return e == cudaSuccess ? per_sm * num_sms : 0;
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s) {
     dim3 grid(a.splits, a.n, a.B);
-    if (a.d == 64) return launch_pdl(attn_decode_kernel<64>, grid, dim3(kAttnThreads), s, a);
-    if (a.d == 128) return launch_pdl(attn_decode_kernel<128>, grid, dim3(kAttnThreads), s, a);
+    if (a.d == 64) return launch_pdl(attn_decode_kernel<64, 1>, grid, dim3(kAttnThreads), s, a);
+    if (a.d == 128) {
+        if ((long long)a.splits * a.n * a.B > a.resident_ctas)
+            return launch_pdl(attn_decode_kernel<128, kAttnCappedMinBlocks>, grid, dim3(kAttnThreads), s, a);
+        return launch_pdl(attn_decode_kernel<128, 1>, grid, dim3(kAttnThreads), s, a);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -195,12 +195,20 @@ struct AttnDecodeArgs {
     int len_host = 0;
     int B = 0, n = 0, d = 0, max_seq = 0;
     int splits = 1;
+    // the lengths, the activity and every key below the length were written before
+    // the previous kernel started (a decode step replayed as a graph): the kernel
+    // loads them before it waits for the previous kernel
+    int early = 0;
+    // CTAs of the unbounded-register d = 128 kernel resident at once (larger grids
+    // take the register-capped form); attn_decode_resident_ctas
+    long long resident_ctas = 0;
     float scale = 0.f;               // 1/sqrt(d)
     float *part = nullptr;           // [B][n][splits][d + 2]
     int *ticket = nullptr;           // [B][n], zero at rest
     uint16_t *o = nullptr;           // [B][n*d]
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s);
+int attn_decode_resident_ctas(int d, int num_sms);
 
 // Per-member temperature + top-p sampling of B rows of float32 logits
 // (k_sample.cu): row b's logits at logits + b * ld, its temperature, top-p and
