@@ -17,24 +17,29 @@
 
 namespace bloom {
 
-template <typename TIn>
+template <int CH, typename TIn>
 __global__ void __launch_bounds__(kLnThreads)
 layernorm_kernel(const TIn *x, const uint16_t *g, const uint16_t *b, int h, float eps,
                  uint16_t *y, int src_stride, const int *last) {
     __shared__ float red[kLnWarps];
     griddep_launch();
+    LnAffine<CH> p;
+    ln_affine_load(g, b, h, p);
     griddep_wait();
     const int r = blockIdx.x;
     const size_t src_row = (size_t)r * src_stride + (last ? last[r] : 0);
-    ln_row(x + src_row * h, g, b, h, eps, y + (size_t)r * h, red);
+    ln_row(x + src_row * h, p, h, eps, y + (size_t)r * h, red);
 }
 
+template <int CH>
 __global__ void __launch_bounds__(kLnThreads)
 embed_kernel(const int *tokens, const uint16_t *emb, int vocab, const uint16_t *g,
              const uint16_t *b, int h, float eps, float *x, const int *len, const int *active,
              const int *next_pos, int *pos, int max_seq, int *err) {
     __shared__ float red[kLnWarps];
     griddep_launch();
+    LnAffine<CH> p;
+    ln_affine_load(g, b, h, p);
     griddep_wait();
     const int r = blockIdx.x;
     int tok = tokens[r];
@@ -47,7 +52,7 @@ embed_kernel(const int *tokens, const uint16_t *emb, int vocab, const uint16_t *
         if (slot >= 0 && slot < max_seq) pos[(size_t)r * max_seq + slot] = next_pos[r];
         else atomicOr(err, kErrSlot);
     }
-    ln_row(emb + (size_t)tok * h, g, b, h, eps, x + (size_t)r * h, red);
+    ln_row(emb + (size_t)tok * h, p, h, eps, x + (size_t)r * h, red);
 }
 
 __global__ void slot_pos_kernel(int B, const int *len, const int *active, const int *next_pos,
@@ -103,20 +108,34 @@ __global__ void set_rows_kernel(const RowList rl, int *dst) {
     if (i < rl.n) dst[i] = rl.rows[i];
 }
 
+template <typename TIn>
+static cudaError_t launch_ln(const TIn *x, const uint16_t *g, const uint16_t *b, int rows, int h,
+                             float eps, uint16_t *y, int src_stride, const int *last,
+                             cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    switch (ln_chunks(h)) {
+    case 2:
+        return launch_pdl(layernorm_kernel<2, TIn>, dim3(rows), dim3(kLnThreads), s, x, g, b, h,
+                          eps, y, src_stride, last);
+    case 4:
+        return launch_pdl(layernorm_kernel<4, TIn>, dim3(rows), dim3(kLnThreads), s, x, g, b, h,
+                          eps, y, src_stride, last);
+    default:
+        return launch_pdl(layernorm_kernel<kLnChunks, TIn>, dim3(rows), dim3(kLnThreads), s, x, g,
+                          b, h, eps, y, src_stride, last);
+    }
+}
+
 cudaError_t launch_layernorm(const uint16_t *x, const uint16_t *g, const uint16_t *b, int rows,
                              int h, float eps, uint16_t *y, int src_stride, const int *last,
                              cudaStream_t s) {
-    if (rows <= 0) return cudaSuccess;
-    return launch_pdl(layernorm_kernel<uint16_t>, dim3(rows), dim3(kLnThreads), s, x, g, b, h, eps,
-                      y, src_stride, last);
+    return launch_ln(x, g, b, rows, h, eps, y, src_stride, last, s);
 }
 
 cudaError_t launch_layernorm_f32(const float *x, const uint16_t *g, const uint16_t *b, int rows,
                                  int h, float eps, uint16_t *y, int src_stride, const int *last,
                                  cudaStream_t s) {
-    if (rows <= 0) return cudaSuccess;
-    return launch_pdl(layernorm_kernel<float>, dim3(rows), dim3(kLnThreads), s, x, g, b, h, eps, y,
-                      src_stride, last);
+    return launch_ln(x, g, b, rows, h, eps, y, src_stride, last, s);
 }
 
 cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int vocab,
@@ -124,8 +143,17 @@ cudaError_t launch_embed(const int *tokens, int n, const uint16_t *emb, int voca
                          const int *len, const int *active, const int *next_pos, int *pos,
                          int max_seq, int *err, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    return launch_pdl(embed_kernel, dim3(n), dim3(kLnThreads), s, tokens, emb, vocab, g, b, h, eps,
-                      x, len, active, next_pos, pos, max_seq, err);
+    switch (ln_chunks(h)) {
+    case 2:
+        return launch_pdl(embed_kernel<2>, dim3(n), dim3(kLnThreads), s, tokens, emb, vocab, g, b,
+                          h, eps, x, len, active, next_pos, pos, max_seq, err);
+    case 4:
+        return launch_pdl(embed_kernel<4>, dim3(n), dim3(kLnThreads), s, tokens, emb, vocab, g, b,
+                          h, eps, x, len, active, next_pos, pos, max_seq, err);
+    default:
+        return launch_pdl(embed_kernel<kLnChunks>, dim3(n), dim3(kLnThreads), s, tokens, emb,
+                          vocab, g, b, h, eps, x, len, active, next_pos, pos, max_seq, err);
+    }
 }
 
 cudaError_t launch_slot_pos(int B, const int *len, const int *active, const int *next_pos,
