@@ -103,16 +103,15 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
     }
     if (a.early) griddep_wait();   // q, and the new key's K / V / position, come from this step
 
-    float qf[EPT], acc[EPT];
+    // q stays packed bf16 (widened per use, exact); the scale multiplies the dot product
+    uint4 qv[EPT / 8];
+    float acc[EPT];
     {
         const uint16_t *qp = a.q + bh * D + sub * EPT;
 #pragma unroll
-        for (int i = 0; i < EPT; i += 8) unpack8(*reinterpret_cast<const uint4 *>(qp + i), qf + i);
+        for (int i = 0; i < EPT / 8; ++i) qv[i] = *reinterpret_cast<const uint4 *>(qp + 8 * i);
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-            qf[e] *= a.scale;
-            acc[e] = 0.f;
-        }
+        for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
     }
     float m_run = -INFINITY, l_run = 0.f;
     const int rounds = (k1 - k0 + KPG * NG - 1) / (KPG * NG);
@@ -131,15 +130,16 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
             if (live[u]) {
 #pragma unroll
                 for (int i = 0; i < EPT / 8; ++i) {
-                    float f[8];
+                    float f[8], qq[8];
                     unpack8(kv[u][i], f);
+                    unpack8(qv[i], qq);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) d = fmaf(qf[8 * i + e], f[e], d);
+                    for (int e = 0; e < 8; ++e) d = fmaf(qq[e], f[e], d);
                 }
             }
 #pragma unroll
             for (int o = 4; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            sc[u] = (live[u] && pk[u] >= 0) ? d + slope * (float)pk[u] : -INFINITY;
+            sc[u] = (live[u] && pk[u] >= 0) ? fmaf(d, a.scale, slope * (float)pk[u]) : -INFINITY;
         }
         float m_new = m_run;
 #pragma unroll
@@ -189,25 +189,32 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
         }
     }
     __syncthreads();
+    // column c of the block's output: the warps' accumulators rescaled to the block maximum
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.m[w]);
-    float L = 0.f, A = 0.f;
-    if (tid < D && M != -INFINITY) {
+    float L = 0.f, wg[NW];
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            if (sm.m[w] == -INFINITY) continue;
-            const float wgt = expf(sm.m[w] - M);
-            L = fmaf(sm.l[w], wgt, L);
-            A = fmaf(sm.acc[w][tid], wgt, A);
-        }
+    for (int w = 0; w < NW; ++w) {
+        wg[w] = 0.f;
+        if (M == -INFINITY || sm.m[w] == -INFINITY) continue;
+        wg[w] = expf(sm.m[w] - M);
+        L = fmaf(sm.l[w], wg[w], L);
     }
+    auto col = [&](int c) {
+        float A = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            if (wg[w] != 0.f) A = fmaf(sm.acc[w][c], wg[w], A);
+        return A;
+    };
     if (splits == 1) {
-        if (tid < D) a.o[(size_t)b * a.n * D + (size_t)j * D + tid] = f2bf(L > 0.f ? A / L : 0.f);
+        for (int c = tid; c < D; c += NT)
+            a.o[(size_t)b * a.n * D + (size_t)j * D + c] = f2bf(L > 0.f ? col(c) / L : 0.f);
         return;
     }
     float *part = a.part + (bh * a.splits + split) * (D + 2);
-    if (tid < D) part[2 + tid] = A;
+    for (int c = tid; c < D; c += NT) part[2 + c] = col(c);
     if (tid == 0) {
         part[0] = M;
         part[1] = L;
@@ -218,10 +225,10 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
-    if (tid < D) {
-        const float *pb = a.part + bh * a.splits * (D + 2);
-        float Mx = -INFINITY;
-        for (int sp = 0; sp < splits; ++sp) Mx = fmaxf(Mx, __ldcg(pb + sp * (D + 2)));
+    const float *pb = a.part + bh * a.splits * (D + 2);
+    float Mx = -INFINITY;
+    for (int sp = 0; sp < splits; ++sp) Mx = fmaxf(Mx, __ldcg(pb + sp * (D + 2)));
+    for (int c = tid; c < D; c += NT) {
         float Ls = 0.f, As = 0.f;
         if (Mx != -INFINITY) {
             for (int sp = 0; sp < splits; ++sp) {
@@ -229,10 +236,10 @@ __device__ __forceinline__ void attn_decode_block(const AttnDecodeArgs &a, int s
                 if (ms == -INFINITY) continue;
                 const float wgt = expf(ms - Mx);
                 Ls = fmaf(__ldcg(pb + sp * (D + 2) + 1), wgt, Ls);
-                As = fmaf(__ldcg(pb + sp * (D + 2) + 2 + tid), wgt, As);
+                As = fmaf(__ldcg(pb + sp * (D + 2) + 2 + c), wgt, As);
             }
         }
-        a.o[(size_t)b * a.n * D + (size_t)j * D + tid] = f2bf(Ls > 0.f ? As / Ls : 0.f);
+        a.o[(size_t)b * a.n * D + (size_t)j * D + c] = f2bf(Ls > 0.f ? As / Ls : 0.f);
     }
     if (tid == 0) a.ticket[bh] = 0;
 }

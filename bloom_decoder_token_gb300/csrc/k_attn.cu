@@ -23,36 +23,36 @@ constexpr int kAttnThreads = 128;
 // takes one contiguous key range (attn_decode_block, which also waits for the
 // previous kernel).
 // ---------------------------------------------------------------------------
-template <int D, int MINB>
-__global__ void __launch_bounds__(kAttnThreads, MINB) attn_decode_kernel(const AttnDecodeArgs a) {
-    __shared__ AttnSmem<D, kAttnThreads> sm;
+template <int D, int NT, int MINB>
+__global__ void __launch_bounds__(NT, MINB) attn_decode_kernel(const AttnDecodeArgs a) {
+    __shared__ AttnSmem<D, NT> sm;
     griddep_launch();
-    attn_decode_block<D, kAttnThreads>(a, blockIdx.x, blockIdx.y, blockIdx.z, sm);
+    attn_decode_block<D, NT>(a, blockIdx.x, blockIdx.y, blockIdx.z, sm);
 }
 
-// Two register budgets for d = 128: unbounded (about 105 registers, four CTAs an
-// SM) where the whole grid is resident at once, else capped for six CTAs an SM
-// (80 registers, no spills).  Measured on GB300 (7b1, 30 layers, decode step):
-// 1 / 8 sequences (128 / 512 CTAs) 3.081 / 2.988 ms unbounded vs 3.088 / 3.023
-// capped; 32 sequences (1024 CTAs) 3.495 vs 3.475; a cap of 64 registers (eight
-// CTAs an SM) spills and took 3.133 / 3.151 / 3.626 ms.
-constexpr int kAttnCappedMinBlocks = 6;
+// Grids larger than the 128-thread CTAs resident at once (about four an SM at
+// ~106 registers) run 64-thread CTAs instead: half the keys per round but all of
+// the grid resident together.  Measured on GB300 (7b1, 30 layers, decode step at
+// 32 sequences, 1024 CTAs): 3.260 ms vs 3.351 with 128-thread CTAs capped at 80
+// registers (six an SM) and 3.495 uncapped; at 64 sequences (2048 CTAs) 4.265
+// vs 4.275.  A 64-register cap (eight 128-thread CTAs an SM) spills: 3.626 ms.
+constexpr int kAttnWideThreads = 64;
 
 int attn_decode_resident_ctas(int d, int num_sms) {
     int per_sm = 0;
     const cudaError_t e = d == 128
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<128, 1>, kAttnThreads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<64, 1>, kAttnThreads, 0);
+        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<128, kAttnThreads, 1>, kAttnThreads, 0)
+        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<64, kAttnThreads, 1>, kAttnThreads, 0);
     return e == cudaSuccess ? per_sm * num_sms : 0;
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s) {
     dim3 grid(a.splits, a.n, a.B);
-    if (a.d == 64) return launch_pdl(attn_decode_kernel<64, 1>, grid, dim3(kAttnThreads), s, a);
+    if (a.d == 64) return launch_pdl(attn_decode_kernel<64, kAttnThreads, 1>, grid, dim3(kAttnThreads), s, a);
     if (a.d == 128) {
         if ((long long)a.splits * a.n * a.B > a.resident_ctas)
-            return launch_pdl(attn_decode_kernel<128, kAttnCappedMinBlocks>, grid, dim3(kAttnThreads), s, a);
-        return launch_pdl(attn_decode_kernel<128, 1>, grid, dim3(kAttnThreads), s, a);
+            return launch_pdl(attn_decode_kernel<128, kAttnWideThreads, 1>, grid, dim3(kAttnWideThreads), s, a);
+        return launch_pdl(attn_decode_kernel<128, kAttnThreads, 1>, grid, dim3(kAttnThreads), s, a);
     }
     return cudaErrorInvalidValue;
 }

@@ -199,8 +199,8 @@ struct AttnDecodeArgs {
     // the previous kernel started (a decode step replayed as a graph): the kernel
     // loads them before it waits for the previous kernel
     int early = 0;
-    // CTAs of the unbounded-register d = 128 kernel resident at once (larger grids
-    // take the register-capped form); attn_decode_resident_ctas
+    // 128-thread CTAs of the d = 128 kernel resident at once (larger grids take
+    // 64-thread CTAs); attn_decode_resident_ctas
     long long resident_ctas = 0;
     float scale = 0.f;               // 1/sqrt(d)
     float *part = nullptr;           // [B][n][splits][d + 2]

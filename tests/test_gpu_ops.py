@@ -152,6 +152,8 @@ def attn_ref(q, k, v, pos, slopes, length):
     (2, 112, 128, 132, 131, 0, 0, ()),     # 176B-shape heads (non-power-of-two slopes)
     (2, 4, 128, 300, 299, 16, 40, (41, 100)),
     (1, 2, 64, 200, 130, 7, 64, ()),       # several splits fully masked
+    (32, 32, 128, 120, 66, 1, 3, (5,)),    # 1024 CTAs: more than are resident at once
+    (8, 112, 128, 140, 100, 1, 0, ()),     # 176B-shape heads, 896 CTAs
 ])
 def test_attn_decode(B, n, d, S, length, splits, pads, holes):
     g = gen(B * 31 + n + d + S + length + splits)
