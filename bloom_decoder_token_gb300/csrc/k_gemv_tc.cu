@@ -530,8 +530,15 @@ int gemv_tc_splits(int N, int K, int M, int epi, int num_sms, int int8) {
     const int tiles = (N + kGvRows - 1) / kGvRows;
     const int kb = int8 ? 128 : kGvBK;   // k per stage
     const int nkb = (K + kb - 1) / kb;
+    // >= 1.5 CTAs per SM; >= 1.25 for QKV, so that more SMs keep a slot for the
+    // attention kernel, which starts early beside it.  Measured on GB300 (7b1,
+    // 30 layers, decode step at 32 / 8 sequences): QKV in 2 splits 3.282 / 2.853 ms
+    // vs 3 splits 3.298 / 2.877 (4: 3.405 / 2.967); dense in 4 / 6 / 8 splits
+    // 3.336 / 3.322 / 3.298 at 32; down in 4 / 8 / 12 3.449 / 3.298 / 3.426; up
+    // in 1 / 2 / 3 3.348 / 3.298 / 3.464.
+    const int num = epi == EPI_QKV ? 5 : 3, den = epi == EPI_QKV ? 4 : 2;
     int s = 1;
-    while (s < kGvMaxSplits && 2 * tiles * s < 3 * num_sms) ++s;        // >= 1.5 CTAs per SM
+    while (s < kGvMaxSplits && den * tiles * s < num * num_sms) ++s;
     while (s > 1 && (tiles * s > 2 * num_sms || nkb / s < kGvMinKbPerSplit)) --s;
     return s;
 }
