@@ -141,7 +141,7 @@ struct bloom_model {
     std::vector<bloom_layer_weights> layers;
     int dev = 0, num_sms = 0;
     int d = 0;
-    long long attn_resident = 0;   // attn_decode_resident_ctas
+    long long attn_resident = 0, attn_resident_wide = 0;   // attn_decode_resident_ctas
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *x = nullptr;           // float32 residual stream [max_tokens][h]
@@ -285,8 +285,10 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     m->d = h / cfg->n_head;
     cudaError_t e = cudaGetDevice(&m->dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->dev);
-    if (e == cudaSuccess && (m->d == 64 || m->d == 128))
+    if (e == cudaSuccess && (m->d == 64 || m->d == 128)) {
         m->attn_resident = attn_decode_resident_ctas(m->d, m->num_sms);
+        m->attn_resident_wide = attn_decode_resident_ctas(m->d, m->num_sms, 1);
+    }
     if (e != cudaSuccess) {
         delete m;
         return fail(BLOOM_E_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
@@ -782,6 +784,10 @@ static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int ma
         at.splits = splits;
         at.early = (g_capture && g_pdl) ? 1 : 0;
         at.resident_ctas = m->attn_resident;
+        at.resident_wide = m->attn_resident_wide;
+        at.bulk = l < kp.offload_from ? 1 : 0;   // the layer's K / V in device memory
+        at.err = m->err;
+        at.wait_ns = (unsigned long long)m->cfg.wait_us * 1000ull;
         at.scale = (float)(1.0 / sqrt((double)d));
         at.part = m->attn_part;
         at.ticket = m->attn_ticket;
@@ -1334,6 +1340,14 @@ extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
     a.splits = splits;
     a.scale = (float)(1.0 / sqrt((double)d));
     a.resident_ctas = attn_decode_resident_ctas(d, device_sms());
+    a.resident_wide = attn_decode_resident_ctas(d, device_sms(), 1);
+    {   // bulk copies only from device memory
+        cudaPointerAttributes pk{}, pv{};
+        a.bulk = cudaPointerGetAttributes(&pk, k_cache) == cudaSuccess &&
+                 cudaPointerGetAttributes(&pv, v_cache) == cudaSuccess &&
+                 pk.type == cudaMemoryTypeDevice && pv.type == cudaMemoryTypeDevice;
+        cudaGetLastError();
+    }
     void *scratch = nullptr;
     const size_t part_bytes = align256((size_t)B * n_head * splits * (d + 2) * 4);
     const size_t bytes = part_bytes + (size_t)B * n_head * 4;

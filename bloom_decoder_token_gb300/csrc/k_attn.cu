@@ -32,17 +32,35 @@ __global__ void __launch_bounds__(NT, MINB) attn_decode_kernel(const AttnDecodeA
 
 // Grids larger than the 128-thread CTAs resident at once (about four an SM at
 // ~106 registers) run 64-thread CTAs instead: half the keys per round but all of
-// the grid resident together.  Measured on GB300 (7b1, 30 layers, decode step at
+// the grid resident together.  Grids larger still (beyond the 64-thread CTAs
+// resident at once) over a cache in device memory take the bulk-staged form
+// (attn_decode_block_bulk): 7b1 at 64 / 128 sequences 4.179 / 5.605 ms per step
+// vs 4.230 / 5.686; at 32 sequences, where the grid fits, 3.307 vs 3.284 (its
+// 27 KB of shared memory keep its CTAs from starting beside the QKV kernel).  Measured on GB300 (7b1, 30 layers, decode step at
 // 32 sequences, 1024 CTAs): 3.260 ms vs 3.351 with 128-thread CTAs capped at 80
 // registers (six an SM) and 3.495 uncapped; at 64 sequences (2048 CTAs) 4.265
 // vs 4.275.  A 64-register cap (eight 128-thread CTAs an SM) spills: 3.626 ms.
 constexpr int kAttnWideThreads = 64;
 
-int attn_decode_resident_ctas(int d, int num_sms) {
+template <int D>
+__global__ void __launch_bounds__(kAttnWideThreads, 1) attn_decode_bulk_kernel(const AttnDecodeArgs a) {
+    __shared__ AttnSmemBulk<D> sm;
+    griddep_launch();
+    attn_decode_block_bulk<D>(a, blockIdx.x, blockIdx.y, blockIdx.z, sm);
+}
+
+int attn_decode_resident_ctas(int d, int num_sms, int wide) {
     int per_sm = 0;
-    const cudaError_t e = d == 128
-        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<128, kAttnThreads, 1>, kAttnThreads, 0)
-        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<64, kAttnThreads, 1>, kAttnThreads, 0);
+    cudaError_t e;
+    if (d == 128 && wide)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<128, kAttnWideThreads, 1>,
+                                                          kAttnWideThreads, 0);
+    else if (d == 128)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<128, kAttnThreads, 1>,
+                                                          kAttnThreads, 0);
+    else
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_decode_kernel<64, kAttnThreads, 1>,
+                                                          kAttnThreads, 0);
     return e == cudaSuccess ? per_sm * num_sms : 0;
 }
 
@@ -50,7 +68,10 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s) {
     dim3 grid(a.splits, a.n, a.B);
     if (a.d == 64) return launch_pdl(attn_decode_kernel<64, kAttnThreads, 1>, grid, dim3(kAttnThreads), s, a);
     if (a.d == 128) {
-        if ((long long)a.splits * a.n * a.B > a.resident_ctas)
+        const long long ctas = (long long)a.splits * a.n * a.B;
+        if (ctas > a.resident_wide && a.bulk)
+            return launch_pdl(attn_decode_bulk_kernel<128>, grid, dim3(kAttnWideThreads), s, a);
+        if (ctas > a.resident_ctas)
             return launch_pdl(attn_decode_kernel<128, kAttnWideThreads, 1>, grid, dim3(kAttnWideThreads), s, a);
         return launch_pdl(attn_decode_kernel<128, kAttnThreads, 1>, grid, dim3(kAttnThreads), s, a);
     }

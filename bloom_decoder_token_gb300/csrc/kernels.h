@@ -202,13 +202,19 @@ struct AttnDecodeArgs {
     // 128-thread CTAs of the d = 128 kernel resident at once (larger grids take
     // 64-thread CTAs); attn_decode_resident_ctas
     long long resident_ctas = 0;
+    long long resident_wide = 0;       // the same for the 64-thread form
+    // K and V in device memory: grids beyond resident_wide stage them by bulk
+    // copies (attn_decode_block_bulk); host-resident (offloaded) caches are read directly
+    int bulk = 0;
+    int *err = nullptr;                // device flag word (8: a bounded wait expired)
+    unsigned long long wait_ns = 0;    // bound of its waits (0: about 2 s)
     float scale = 0.f;               // 1/sqrt(d)
     float *part = nullptr;           // [B][n][splits][d + 2]
     int *ticket = nullptr;           // [B][n], zero at rest
     uint16_t *o = nullptr;           // [B][n*d]
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, cudaStream_t s);
-int attn_decode_resident_ctas(int d, int num_sms);
+int attn_decode_resident_ctas(int d, int num_sms, int wide = 0);
 
 // Per-member temperature + top-p sampling of B rows of float32 logits
 // (k_sample.cu): row b's logits at logits + b * ld, its temperature, top-p and

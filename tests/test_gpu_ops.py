@@ -154,6 +154,8 @@ def attn_ref(q, k, v, pos, slopes, length):
     (1, 2, 64, 200, 130, 7, 64, ()),       # several splits fully masked
     (32, 32, 128, 120, 66, 1, 3, (5,)),    # 1024 CTAs: more than are resident at once
     (8, 112, 128, 140, 100, 1, 0, ()),     # 176B-shape heads, 896 CTAs
+    (64, 32, 128, 140, 100, 1, 2, (7,)),   # 2048 CTAs: K / V staged by bulk copies
+    (16, 112, 128, 300, 280, 2, 0, ()),    # 3584 CTAs, two splits merged by the last
 ])
 def test_attn_decode(B, n, d, S, length, splits, pads, holes):
     g = gen(B * 31 + n + d + S + length + splits)
