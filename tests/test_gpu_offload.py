@@ -65,6 +65,27 @@ def test_offloaded_cache_is_bit_identical(offload_from):
     gm.close()
 
 
+def test_offloaded_cache_is_bit_identical_where_device_layers_stage_kv_by_bulk_copies():
+    # 7b1 heads (32 x 128) at 48 sequences: 1536 attention CTAs, beyond the 64-thread
+    # CTAs resident at once, so the device-resident layer stages its K / V by bulk
+    # copies while the host-resident one reads them directly -- the same bits
+    shape = synth.PRESETS["7b1"].with_(n_layer=2, vocab=1000, batch=48, prompt=20, ragged=True)
+    w = synth.make_weights(shape, seed=74, random_affine=True).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=74)
+    B, T = ids.shape
+    S = T + 4
+    gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S)
+    kv_d = gm.new_kv(B, S)
+    kv_h = gm.new_kv(B, S, offload_from=1)
+    ref = run(gm, kv_d, ids, mask, 3, shape.vocab)
+    got = run(gm, kv_h, ids, mask, 3, shape.vocab)
+    for (t0, l0), (t1, l1) in zip(ref, got):
+        assert torch.equal(t0, t1)
+        assert torch.equal(l0, l1)
+    gm.check_device()
+    gm.close()
+
+
 def test_offloaded_generation_against_oracle():
     shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000, batch=3, prompt=8, ragged=True)
     w = synth.make_weights(shape, seed=72, random_affine=True)
