@@ -72,9 +72,10 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
     return d;
 }
 
-// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B (f16 A and B
+// with f16 set: the two operands always share one type), both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc(int m, int n, bool f16 = false) {
+    return (1u << 4) | (f16 ? 0u : ((1u << 7) | (1u << 10))) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
 }
 

@@ -40,6 +40,34 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int i) {
     return o;
 }
 
+// Two int8 codes (bytes i, i+1 of w) -> f16x2, exactly.  With the sign bits
+// flipped (w ^ 0x80808080), one byte permute places q + 128 as the low
+// mantissa byte of two halves 1024 + (q + 128) (high byte 0x64), and one paired
+// half subtraction removes 1152 (|q| <= 128 is exact in f16).  Two
+// instructions per pair, the flip shared by a word's two pairs.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t w, int i) {
+    const uint32_t wx = w ^ 0x80808080u;
+    uint32_t h, o;
+    asm("prmt.b32 %0, %1, %2, %3;"
+        : "=r"(h)
+        : "r"(wx), "r"(0x64646464u), "r"(0x4040u | (uint32_t)i | ((uint32_t)(i + 1) << 8)));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o) : "r"(h), "r"(0x64806480u));
+    return o;
+}
+
+// Eight bf16 -> eight f16 (round to nearest; exact for |x| in [2^-14, 65504],
+// where f16 holds every bf16 value).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    auto cv = [](uint32_t w) {
+        uint32_t o;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;"
+            : "=r"(o)
+            : "f"(__uint_as_float(w & 0xffff0000u)), "f"(__uint_as_float(w << 16)));
+        return o;
+    };
+    return make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
+}
+
 // LayerNorm of the M float32 rows a.ln_x[M][K] into shared memory as bf16
 // (row pitch px bytes), the register-lean form for kernels whose occupancy
 // matters more than the latency of the prologue: float32 statistics, biased
