@@ -251,8 +251,9 @@ def test_linear_tc_176b_shapes_sampled(N, K, M):
 
 
 # ---------------------------------------------------------------- int8 on the tensor-core decode kernel
-# int8 codes are widened exactly to bf16 into a TMEM A operand; ragged N, a K
-# tail that is not a multiple of the 128-wide int8 k-block, split and unsplit.
+# int8 codes are widened exactly into a TMEM A operand (f16 with the activations
+# converted to f16 up to 32 token columns, bf16 above); ragged N, a K tail that
+# is not a multiple of the 128-wide int8 k-block, split and unsplit.
 INT8_TC_SHAPES = [(3, 300, 192), (8, 3072, 1024), (17, 520, 1040), (32, 4096, 4096),
                   (64, 1040, 2048), (100, 256, 16384), (128, 12288, 4096), (33, 128, 64)]
 
@@ -280,17 +281,18 @@ def test_linear_tc_int8(M, N, K, epi):
     assert_kernel_close(y, ref, what=f"linear_tc int8 {M}x{N}x{K}")
 
 
-def test_linear_tc_int8_every_code():
+@pytest.mark.parametrize("reps", [1, 2], ids=["f16-form", "bf16-form"])
+def test_linear_tc_int8_every_code(reps):
     """Every int8 code (-128 .. 127), at even and odd k, in every 16-byte chunk of
     the 128-byte swizzled rows and in both 128-wide k-blocks, comes out exactly:
     with unit scales, no bias and one-hot activations y[m][n] = q[n][p_m].  This
-    pins the widening and the order of the two bf16 values in each TMEM column
-    of the A operand."""
+    pins the widening and the order of the two 16-bit values in each TMEM column
+    of the A operand, in the f16 form (20 token columns) and the bf16 form (40)."""
     N, K = 512, 256
     n = torch.arange(N).unsqueeze(1)
     k = torch.arange(K).unsqueeze(0)
     q = ((3 * n + k) % 256).to(torch.uint8).view(torch.int8)
-    pos = [0, 1, 2, 3, 14, 15, 16, 17, 31, 62, 63, 64, 65, 100, 127, 128, 129, 200, 254, 255]
+    pos = [0, 1, 2, 3, 14, 15, 16, 17, 31, 62, 63, 64, 65, 100, 127, 128, 129, 200, 254, 255] * reps
     x = torch.zeros(len(pos), K, dtype=torch.bfloat16)
     for m, p in enumerate(pos):
         x[m, p] = 1.0
