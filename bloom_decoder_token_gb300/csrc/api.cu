@@ -1318,6 +1318,9 @@ extern "C" bloom_status bloom_op_attn_decode(const void *q, const void *k_cache,
     if (d != 64 && d != 128) return fail(BLOOM_E_UNSUPPORTED, "d=%d", d);
     if (B < 1 || n_head < 1 || max_seq < 1 || len < 0 || len >= max_seq)
         return fail(BLOOM_E_INVALID, "B=%d n=%d max_seq=%d len=%d", B, n_head, max_seq, len);
+    // q, K, V and o are read and written 16 bytes at a time (K / V also by bulk copies)
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+        return fail(BLOOM_E_INVALID, "q, k_cache, v_cache and o must be 16-byte aligned");
     if (splits <= 0) {
         int want = (2 * device_sms() + B * n_head - 1) / (B * n_head);
         int cap = (len + 1 + 31) / 32;

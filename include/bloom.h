@@ -369,8 +369,9 @@ bloom_status bloom_op_gemm(const bloom_linear *lin, const void *x, int32_t M, in
  * TMEM; narrow matrices split K over a thread-block cluster whose partials are
  * summed in split order ("DeepSpeed Inference", III.A: small-batch cost is
  * reading W).  int8 = 0: bf16 weights, M <= 256, K % 8 == 0.  int8 = 1: int8
- * codes with bf16 row scales (lin->scale), widened exactly to bf16 on the chip
- * and scaled per row in the epilogue, M <= 128, K % 16 == 0 ("Incredibly Fast
+ * codes with bf16 row scales (lin->scale), widened exactly on the chip (to f16,
+ * with the activations converted to f16, up to 32 rows; to bf16 above) and
+ * scaled per row in the epilogue, M <= 128, K % 16 == 0 ("Incredibly Fast
  * BLOOM Inference...", Key observations: int8 halves the bytes read).  x and
  * lin->w 16-byte aligned.  Same epilogues and result layout as bloom_op_linear. */
 bloom_status bloom_op_linear_tc(const bloom_linear *lin, int32_t int8, const void *x, int32_t M,
@@ -380,7 +381,9 @@ bloom_status bloom_op_linear_tc(const bloom_linear *lin, int32_t int8, const voi
  * q bf16 [B][n][d]; k_cache, v_cache bf16 [B][n][max_seq][d]; pos int32
  * [B][max_seq] (-1 = masked); keys are slots [0, len]; slopes float [n];
  * o bf16 [B][n*d].  d in {64, 128}.  `splits` key ranges per (b, head), 0 =
- * library choice. */
+ * library choice.  q, k_cache, v_cache and o 16-byte aligned (BLOOM_E_INVALID
+ * otherwise); K / V in device memory may be staged by bulk copies, K / V in
+ * host memory are read directly. */
 bloom_status bloom_op_attn_decode(const void *q, const void *k_cache, const void *v_cache,
                                   const int32_t *pos, const float *slopes, int32_t B,
                                   int32_t n_head, int32_t d, int32_t max_seq, int32_t len,

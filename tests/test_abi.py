@@ -107,6 +107,12 @@ def test_ops_reject_bad_arguments(lib):
     assert lib.bloom_op_layernorm(C.c_void_p(16), None, None, 1, 20, 1e-5, C.c_void_p(16), None) == 2
     assert lib.bloom_op_attn_decode(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16),
                                     C.c_void_p(16), 1, 1, 96, 8, 0, 0, C.c_void_p(16), None) == 2
+    # K / V read 16 bytes at a time and by bulk copies: a misaligned cache is rejected
+    # on the host, before any device call
+    assert lib.bloom_op_attn_decode(C.c_void_p(16), C.c_void_p(24), C.c_void_p(16), C.c_void_p(16),
+                                    C.c_void_p(16), 1, 1, 128, 8, 0, 0, C.c_void_p(16), None) == 1
+    assert lib.bloom_op_attn_decode(C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16),
+                                    C.c_void_p(16), 1, 1, 128, 8, 0, 0, C.c_void_p(18), None) == 1
     assert lib.bloom_op_lmhead_argmax(C.c_void_p(16), C.c_void_p(16), 0, 8, 8, C.c_void_p(16),
                                       None, None) == 2
     lin = bg.Linear(C.c_void_p(16), None, None)
