@@ -339,7 +339,20 @@ extern "C" bloom_status bloom_create(const bloom_config *cfg, const bloom_weight
     for (int i = 1; i <= p2; ++i) sl[i - 1] = (float)pow(2.0, -8.0 * i / p2);
     for (int j = 0; j < (int)n - p2; ++j) sl[p2 + j] = (float)pow(2.0, -8.0 * (2 * j + 1) / (2.0 * p2));
     bloom_status st2 = BLOOM_OK;
-    if (cudaMemset(m->ws, 0, m->ws_bytes) != cudaSuccess ||
+    // BLOOM_POISON_WORKSPACE (a debug aid for tests): every byte of the workspace
+    // 0xff (NaN in bf16 and float32, -1 in int32) except the tickets, the argmax
+    // scratch and the flag word, which rest at zero; a kernel that read any
+    // activation before writing it would then show NaN or wrong tokens
+    const bool poison = getenv("BLOOM_POISON_WORKSPACE") != nullptr;
+    auto init_ws = [&]() -> bool {
+        if (!poison) return cudaMemset(m->ws, 0, m->ws_bytes) == cudaSuccess;
+        return cudaMemset(m->ws, 0xff, m->ws_bytes) == cudaSuccess &&
+               cudaMemset(base + o_best, 0, MB * 8) == cudaSuccess &&
+               cudaMemset(base + o_ht, 0, 4) == cudaSuccess &&
+               cudaMemset(base + o_at, 0, MB * n * 4) == cudaSuccess &&
+               cudaMemset(base + o_err, 0, 4) == cudaSuccess;
+    };
+    if (!init_ws() ||
         cudaMemcpy(m->slopes, sl.data(), n * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking) != cudaSuccess ||
         linear_prepare() != cudaSuccess) {

@@ -150,7 +150,11 @@ size_t bloom_kv_bytes(const bloom_config *cfg, int32_t batch, int32_t max_seq);
  * sequence), allocate the activation workspace, and pick launch shapes.
  * The current CUDA device is the model's device.  *out is NULL on failure.
  * For testing the error path, the environment variable BLOOM_INJECT_FAILURE
- * containing "workspace" makes the workspace allocation fail (BLOOM_E_OOM). */
+ * containing "workspace" makes the workspace allocation fail (BLOOM_E_OOM).
+ * For testing that no kernel reads an activation before writing it, the
+ * variable BLOOM_POISON_WORKSPACE fills the workspace with 0xff bytes (NaN in
+ * bf16 and float32) instead of zeros, all but its tickets, argmax scratch and
+ * flag word; results must not change. */
 bloom_status bloom_create(const bloom_config *cfg, const bloom_weights *w, bloom_model **out);
 
 /* Bind `buf` (device, >= bloom_kv_bytes bytes, 256-byte aligned) as an empty

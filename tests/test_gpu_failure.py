@@ -7,6 +7,8 @@
   model with the default bound then decodes against the oracle.
 * Host-side injection: BLOOM_INJECT_FAILURE=workspace makes bloom_create's
   workspace allocation fail with BLOOM_E_OOM, and the next create succeeds.
+* Poisoned workspace: BLOOM_POISON_WORKSPACE fills the workspace with NaN bytes
+  instead of zeros; generations are bit-identical.
 """
 import pytest
 import torch
@@ -69,6 +71,40 @@ def test_expired_waits_are_reported_and_the_device_stays_usable():
     gm2.close()
     # the same device, the default bound: correct against the oracle
     generate_parity(shape, w, steps=3, tol=2e-2)
+
+
+def test_poisoned_workspace_changes_nothing(monkeypatch):
+    """BLOOM_POISON_WORKSPACE: the workspace starts as 0xff bytes (NaN in bf16
+    and float32) instead of zeros.  A prefill and decode steps -- streaming and
+    tensor-core linears, split-K partials, attention partials, LayerNorms, the
+    head's argmax -- give bit-identical logits and tokens, so no kernel reads an
+    activation or a partial before writing it."""
+    shape = synth.PRESETS["560m"].with_(n_layer=2, vocab=3000, batch=6, prompt=8, ragged=True)
+    w = synth.make_weights(shape, seed=64, random_affine=True).to(DEV)
+    ids, mask = synth.make_prompts(shape, seed=64)
+    B, T = ids.shape
+    S = T + 5
+    outs = []
+    for poison in (False, True):
+        if poison:
+            monkeypatch.setenv("BLOOM_POISON_WORKSPACE", "1")
+        gm = bg.Model(w, max_batch=B, max_tokens=B * T, max_seq=S)
+        monkeypatch.delenv("BLOOM_POISON_WORKSPACE", raising=False)
+        kv = gm.new_kv(B, S)
+        lg = torch.empty(B, shape.vocab, dtype=torch.float32, device=DEV)
+        tok = gm.prefill(kv, ids.to(DEV), mask.to(DEV), logits=lg)
+        run = [(tok.clone(), lg.clone())]
+        for _ in range(4):
+            tok = gm.decode_step(kv, tok, logits=lg)
+            run.append((tok.clone(), lg.clone()))
+        torch.cuda.synchronize()
+        gm.check_device()
+        gm.close()
+        outs.append(run)
+    for (t0, l0), (t1, l1) in zip(*outs):
+        assert torch.isfinite(l1).all()
+        assert torch.equal(t0, t1)
+        assert torch.equal(l0, l1)
 
 
 def test_injected_workspace_allocation_failure(monkeypatch):
