@@ -12,6 +12,8 @@
 #include <vector>
 
 #include "../../include/bloom.h"
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.h"
 
 using namespace bloom;
@@ -56,6 +58,15 @@ void bloom::bloom_set_error(const char *fmt, ...) {
 }
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// NVTX ranges around the host-side phases (prefill, decode step, each layer's
+// launches; named in a profiler's timeline, no cost when none is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Host-side fault injection for tests: BLOOM_INJECT_FAILURE names the
 // allocations to fail ("workspace").
@@ -761,6 +772,9 @@ static cudaError_t fused_ln(bloom_model *m, LinearArgs &a, const float *x, const
 static cudaError_t enqueue_layer(bloom_model *m, const KvPtrs &kp, int B, int max_seq, int l,
                                  int M, int T, int splits, float *x, cudaStream_t s,
                                  const int *row_map = nullptr) {
+    char rname[32];
+    snprintf(rname, sizeof rname, "bloom layer %d", l);
+    NvtxRange range(rname);
     const bloom_config &c = m->cfg;
     const bloom_layer_weights &L = m->layers[l];
     const int h = c.hidden, F = c.ffn, n = c.n_head, d = m->d;
@@ -944,6 +958,7 @@ static bloom_status prefill_rows(bloom_model *m, bloom_kv *kv, const int32_t *to
 extern "C" bloom_status bloom_prefill(bloom_model *m, bloom_kv *kv, const int32_t *tokens,
                                       const uint8_t *mask, int32_t B, int32_t T,
                                       int32_t *out_tokens, float *out_logits, void *stream) {
+    NvtxRange range("bloom_prefill");
     if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
@@ -963,6 +978,7 @@ extern "C" bloom_status bloom_kv_admit(bloom_model *m, bloom_kv *kv, const int32
                                        int32_t n, const int32_t *tokens, const uint8_t *mask,
                                        int32_t T, int32_t *out_tokens, float *out_logits,
                                        void *stream) {
+    NvtxRange range("bloom_kv_admit");
     if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
@@ -1006,6 +1022,7 @@ extern "C" bloom_status bloom_kv_retire(bloom_model *m, bloom_kv *kv, const int3
 
 extern "C" bloom_status bloom_decode_step(bloom_model *m, bloom_kv *kv, const int32_t *next_tokens,
                                           int32_t *out_tokens, float *out_logits, void *stream) {
+    NvtxRange range("bloom_decode_step");
     if (m) g_pdl = !(m->cfg.flags & BLOOM_FLAG_NO_PDL);
     bloom_status st = check_kv(m, kv);
     if (st) return st;
@@ -1112,6 +1129,7 @@ extern "C" bloom_status bloom_check_device(bloom_model *m, void *stream) {
 extern "C" bloom_status bloom_generate(bloom_model *m, bloom_kv *kv, const int32_t *tokens_host,
                                        const uint8_t *mask_host, int32_t B, int32_t T,
                                        int32_t n_new, int32_t *out_host, void *stream) {
+    NvtxRange range("bloom_generate");
     bloom_status st = check_kv(m, kv);
     if (st) return st;
     if (!tokens_host || !mask_host || !out_host) return fail(BLOOM_E_INVALID, "null host buffer");
@@ -1405,6 +1423,7 @@ extern "C" bloom_status bloom_decode_step_sampled(bloom_model *m, bloom_kv *kv,
                                                   float *logits, const float *temperature,
                                                   const float *top_p, const float *u,
                                                   void *stream) {
+    NvtxRange range("bloom_decode_step_sampled");
     if (!logits || !temperature || !top_p || !u) return fail(BLOOM_E_INVALID, "null argument");
     bloom_status st = bloom_decode_step(m, kv, next_tokens, out_tokens, logits, stream);
     if (st) return st;
