@@ -22,6 +22,12 @@
 // step is captured once for every length); a block derives the split count it
 // uses from the live key count, at least kAttnMinKeysPerSplit keys a split, and
 // blocks beyond it return at once.
+//
+// Two bodies share the per-round arithmetic (attn_round) and the merge
+// (attn_finish), so they give the same bits: attn_decode_block loads each
+// round's K / V rows into registers; attn_decode_block_bulk (64-thread blocks
+// over a cache in device memory) stages them in shared memory by bulk copies
+// three rounds ahead.
 #pragma once
 
 #include <math.h>

@@ -30,16 +30,18 @@ __global__ void __launch_bounds__(NT, MINB) attn_decode_kernel(const AttnDecodeA
     attn_decode_block<D, NT>(a, blockIdx.x, blockIdx.y, blockIdx.z, sm);
 }
 
-// Grids larger than the 128-thread CTAs resident at once (about four an SM at
-// ~106 registers) run 64-thread CTAs instead: half the keys per round but all of
-// the grid resident together.  Grids larger still (beyond the 64-thread CTAs
-// resident at once) over a cache in device memory take the bulk-staged form
-// (attn_decode_block_bulk): 7b1 at 64 / 128 sequences 4.179 / 5.605 ms per step
-// vs 4.230 / 5.686; at 32 sequences, where the grid fits, 3.307 vs 3.284 (its
-// 27 KB of shared memory keep its CTAs from starting beside the QKV kernel).  Measured on GB300 (7b1, 30 layers, decode step at
-// 32 sequences, 1024 CTAs): 3.260 ms vs 3.351 with 128-thread CTAs capped at 80
-// registers (six an SM) and 3.495 uncapped; at 64 sequences (2048 CTAs) 4.265
-// vs 4.275.  A 64-register cap (eight 128-thread CTAs an SM) spills: 3.626 ms.
+// Three forms by grid size (measured on GB300, 7b1, 30 layers, whole decode step):
+//  * 128-thread CTAs (~106 registers, about four an SM) where the whole grid is
+//    resident at once;
+//  * 64-thread CTAs beyond that: half the keys per round but all of the grid
+//    resident together -- at 32 sequences (1024 CTAs) 3.260 ms vs 3.351 with
+//    128-thread CTAs capped at 80 registers (six an SM) and 3.495 uncapped; a
+//    64-register cap (eight 128-thread CTAs an SM) spills: 3.626 ms;
+//  * beyond the 64-thread CTAs resident at once, over a cache in device memory,
+//    the bulk-staged form (attn_decode_block_bulk): at 64 / 128 sequences 4.179 /
+//    5.605 ms vs 4.230 / 5.686; at 32 sequences, where the grid fits, it lost
+//    (3.307 vs 3.284: its 27 KB of shared memory keep its CTAs from starting
+//    beside the QKV kernel).
 constexpr int kAttnWideThreads = 64;
 
 template <int D>
